@@ -1,0 +1,354 @@
+"""Seeded synthetic inputs for DDTree verify attention over an MLA latent KV pool.
+
+This module holds no attention arithmetic.  It only draws random draft trees,
+simulates a page_size=1 token-slot allocator, samples N(0,1) values rounded to
+bf16 and lays the buffers out.  Both the CUDA path (tests, bench) and the CPU
+oracle take their inputs from here, so neither side generates data for the
+other.
+
+Shapes follow the MLA absorbed form: every KV slot is one 576-wide bf16 latent
+row (512 latent dims + 64 rope dims, 1152 bytes), one KV head, and the tree
+nodes' queries are 576-wide per head ("The Architecture Detective: Uncovering
+FlashMLA's Potential for Blackwell DDTree Verification", section "The Message in
+Full": num_heads_k=1, head_dim=576).
+
+Allocator model ("The Architecture Detective", sections "The Message in Full"
+and "Defragmentation: Separating Signal from Noise"; "The Anatomy of a Kernel
+Investigation", section "The Bash Command: Reading the Source"): the pool starts with a free list of every slot but the padded
+slot 0; alloc(n) hands out the first n entries of the free list and removes
+them; a freed allocation is appended to the end of the list in its own order.
+A fresh pool therefore gives contiguous slots and a churned one gives slots
+that are scattered over the whole pool.
+"""
+from __future__ import annotations
+
+import collections
+import dataclasses
+import math
+
+import numpy as np
+
+D_QK = 576          # q/k width: 512 latent dims + 64 rope dims
+D_V = 512           # v width: the latent part of the same row
+ROW_BYTES = D_QK * 2
+BF16_NAN = 0x7FC0   # quiet NaN used to poison slots no request owns
+
+
+@dataclasses.dataclass(frozen=True)
+class Config:
+    name: str
+    batch: int
+    prefix: tuple            # fixed prefix length per request, or ("uniform", lo, hi)
+    nodes: int               # tree nodes per request (node 0 is the root)
+    tree: str                # "random" or "chain"
+    max_depth: int
+    max_branch: int          # 0 = no cap on children per node
+    heads: int
+    pool_slots: int
+    slots: str               # "perm", "churn" or "contiguous"
+    seed: int
+
+
+CONFIGS = {
+    "tiny": Config("tiny", 1, (256,), 9, "random", 4, 0, 16, 4096, "perm", 0xDD7EE000),
+    "c2": Config("c2", 1, (8192,), 65, "random", 8, 4, 16, 1 << 20, "churn", 0xDD7EE001),
+    "c3": Config("c3", 1, (65536,), 65, "random", 8, 4, 128, 2 << 20, "churn", 0xDD7EE002),
+    "c4": Config("c4", 1, (185000,), 9, "chain", 8, 1, 16, 4 << 20, "perm", 0xDD7EE003),
+    "c5": Config("c5", 8, ("uniform", 4096, 131072), 33, "random", 6, 4, 16, 8 << 20, "churn",
+                 0xDD7EE004),
+}
+
+DESCRIPTIONS = {
+    "tiny": "1 request, prefix 256, 9 random tree nodes (depth<=4), 16 heads, pool 4096, permuted slots",
+    "c2": "1 request, prefix 8192, 65 tree nodes (depth<=8, branching<=4), 16 heads, pool 1M, churned slots",
+    "c3": "1 request, prefix 65536, 65 tree nodes, 128 heads, pool 2M, churned slots",
+    "c4": "1 request, prefix 185000, chain of 9 nodes, 16 heads, pool 4M, permuted slots",
+    "c5": "8 requests, prefixes U[4096,131072], 33 tree nodes each (depth<=6), 16 heads, pool 8M, churned slots",
+}
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); returns uint16 bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounded = u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    out = (rounded >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = BF16_NAN
+    return out
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float32."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal_bf16(rng: np.random.Generator, shape, chunk_rows: int = 1 << 16) -> np.ndarray:
+    """N(0,1) samples rounded to bf16, generated in row chunks to bound host memory."""
+    shape = tuple(int(s) for s in shape)
+    out = np.empty(shape, dtype=np.uint16)
+    flat = out.reshape(-1, shape[-1]) if len(shape) > 1 else out.reshape(1, -1)
+    for r0 in range(0, flat.shape[0], chunk_rows):
+        r1 = min(flat.shape[0], r0 + chunk_rows)
+        flat[r0:r1] = f32_to_bf16_bits(rng.standard_normal((r1 - r0, flat.shape[1]), dtype=np.float32))
+    return out
+
+
+# ----------------------------------------------------------------------------- trees
+
+def random_tree(rng: np.random.Generator, nodes: int, max_depth: int, max_branch: int) -> np.ndarray:
+    """Parent array of a random tree in topological order: parent[0] = -1, parent[i] < i.
+
+    Each new node picks its parent uniformly among the nodes that are still below
+    the depth cap and under the branching cap (0 = uncapped).
+    """
+    parent = np.full(nodes, -1, dtype=np.int32)
+    depth = np.zeros(nodes, dtype=np.int32)
+    children = np.zeros(nodes, dtype=np.int32)
+    for i in range(1, nodes):
+        ok = [j for j in range(i)
+              if depth[j] < max_depth and (max_branch == 0 or children[j] < max_branch)]
+        if not ok:
+            raise ValueError("tree caps leave no room for another node")
+        p = ok[int(rng.integers(len(ok)))]
+        parent[i] = p
+        depth[i] = depth[p] + 1
+        children[p] += 1
+    return parent
+
+
+def chain_tree(nodes: int) -> np.ndarray:
+    return np.arange(-1, nodes - 1, dtype=np.int32)
+
+
+def tree_depths(parent: np.ndarray) -> np.ndarray:
+    d = np.zeros(len(parent), dtype=np.int32)
+    for i in range(1, len(parent)):
+        d[i] = d[parent[i]] + 1
+    return d
+
+
+# ----------------------------------------------------------------------------- allocator
+
+class FreeListAllocator:
+    """page_size=1 token-slot allocator: alloc takes the head of the free list, free appends.
+
+    The free list is kept as a deque of index arrays so that alloc and free cost
+    O(allocation size) even for pools of millions of slots.
+    """
+
+    def __init__(self, pool_slots: int):
+        self.pool_slots = int(pool_slots)
+        self.segments = collections.deque([np.arange(1, pool_slots, dtype=np.int64)])
+        self.free_count = pool_slots - 1
+
+    def alloc(self, n: int) -> np.ndarray:
+        if n > self.free_count:
+            raise MemoryError(f"alloc({n}) with {self.free_count} free slots")
+        parts, need = [], n
+        while need:
+            seg = self.segments[0]
+            if len(seg) <= need:
+                parts.append(seg)
+                need -= len(seg)
+                self.segments.popleft()
+            else:
+                parts.append(seg[:need])
+                self.segments[0] = seg[need:]
+                need = 0
+        self.free_count -= n
+        return np.concatenate(parts) if len(parts) > 1 else parts[0].copy()
+
+    def free(self, slots: np.ndarray) -> None:
+        self.segments.append(np.asarray(slots, dtype=np.int64))
+        self.free_count += len(slots)
+
+
+def churned_allocator(rng: np.random.Generator, pool_slots: int, keep_free: int,
+                      max_alloc: int = 4096, rounds_per_live: int = 4) -> FreeListAllocator:
+    """Simulate serving churn: fill the pool, then repeatedly free a random live
+    allocation and allocate a new one of size U[1, max_alloc].
+
+    At least `keep_free` slots stay free at the end for the measured requests.
+    """
+    a = FreeListAllocator(pool_slots)
+    target_live = max(0, pool_slots - 1 - keep_free)
+    live = []
+    used = 0
+    while True:
+        n = int(rng.integers(1, max_alloc + 1))
+        if used + n > target_live:
+            break
+        live.append(a.alloc(n))
+        used += n
+    for _ in range(rounds_per_live * max(1, len(live))):
+        if not live:
+            break
+        i = int(rng.integers(len(live)))
+        victim = live[i]
+        live[i] = live[-1]
+        live.pop()
+        a.free(victim)
+        used -= len(victim)
+        n = int(rng.integers(1, max_alloc + 1))
+        if used + n <= target_live:
+            live.append(a.alloc(n))
+            used += n
+    return a
+
+
+# ----------------------------------------------------------------------------- workloads
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    batch: int
+    nodes: int
+    heads: int
+    pool_slots: int
+    sm_scale: float
+    prefix_len: np.ndarray          # int32 [B]
+    slot_stride: int
+    slot_idx: np.ndarray            # int32 [B, slot_stride]; row b's first prefix_len[b] entries used
+    tree_parent: np.ndarray         # int32 [B, T]
+    tree_slot_idx: np.ndarray       # int32 [B, T]
+    q_bits: np.ndarray              # uint16 [B, T, H, 576] (bf16)
+    kv_prefix_bits: list            # per request: uint16 [prefix_len[b], 576], logical order
+    kv_tree_bits: np.ndarray        # uint16 [B, T, 576]: tree node rows
+
+    @property
+    def rows_per_request(self) -> int:
+        return self.nodes * self.heads
+
+    @property
+    def max_prefix_len(self) -> int:
+        return int(self.prefix_len.max()) if self.batch else 0
+
+    def kv_bytes(self) -> int:
+        """KV bytes one verify step must read: every prefix and tree row once."""
+        return int((int(self.prefix_len.sum()) + self.batch * self.nodes) * ROW_BYTES)
+
+    def flops(self) -> int:
+        """Algorithmic FLOPs of the prefix contraction: 2*T*H*L*(576+512) per request."""
+        return int(2 * self.nodes * self.heads * int(self.prefix_len.sum()) * (D_QK + D_V))
+
+    def algorithmic_bytes(self) -> int:
+        """KV rows once + slot indices + q + out (fp32) + lse (fp32)."""
+        rows = self.batch * self.nodes * self.heads
+        return (self.kv_bytes() + int(self.prefix_len.sum()) * 4 + self.batch * self.nodes * 8
+                + rows * ROW_BYTES + rows * D_V * 4 + rows * 4)
+
+    def used_slots(self) -> np.ndarray:
+        parts = [self.slot_idx[b, :self.prefix_len[b]] for b in range(self.batch)]
+        parts.append(self.tree_slot_idx.reshape(-1))
+        return np.concatenate(parts).astype(np.int64)
+
+    def compact_host_pool(self):
+        """Small host pool holding only the used rows, plus the slot tables remapped to it.
+
+        Row order: request 0 prefix, request 0 tree, request 1 prefix, ...  The
+        oracle gives the same result on this pool as on the full one (a joint
+        permutation of pool rows and slot indices), which the oracle tests pin.
+        """
+        rows, slot_idx, tree_slot = [], np.zeros_like(self.slot_idx), np.zeros_like(self.tree_slot_idx)
+        off = 0
+        for b in range(self.batch):
+            L = int(self.prefix_len[b])
+            rows.append(self.kv_prefix_bits[b])
+            slot_idx[b, :L] = np.arange(off, off + L, dtype=np.int32)
+            off += L
+            rows.append(self.kv_tree_bits[b])
+            tree_slot[b] = np.arange(off, off + self.nodes, dtype=np.int32)
+            off += self.nodes
+        return np.concatenate(rows, axis=0), slot_idx, tree_slot
+
+
+def _prefix_lengths(cfg: Config, rng: np.random.Generator) -> np.ndarray:
+    if cfg.prefix[0] == "uniform":
+        _, lo, hi = cfg.prefix
+        return rng.integers(lo, hi + 1, size=cfg.batch).astype(np.int32)
+    return np.full(cfg.batch, int(cfg.prefix[0]), dtype=np.int32)
+
+
+def make_workload(name: str, seed: int | None = None, slots: str | None = None,
+                  **overrides) -> Workload:
+    """Build one of the named configurations (see CONFIGS), fully determined by its seed.
+
+    `slots` overrides the slot layout ("perm", "churn", "contiguous") while keeping
+    every value identical, so layouts can be compared output for output.
+    `overrides` may replace Config fields (batch, prefix, nodes, heads, ...) for
+    small test variants.
+    """
+    cfg = CONFIGS[name]
+    if overrides:
+        cfg = dataclasses.replace(cfg, **overrides)
+    seed = cfg.seed if seed is None else seed
+    layout = slots or cfg.slots
+    # independent streams: structure, values and slot layout never perturb one another
+    ss = np.random.SeedSequence(seed)
+    s_struct, s_vals, s_slots = [np.random.Generator(np.random.PCG64(s)) for s in ss.spawn(3)]
+
+    B, T, H = cfg.batch, cfg.nodes, cfg.heads
+    prefix_len = _prefix_lengths(cfg, s_struct)
+    if cfg.tree == "chain":
+        parents = np.stack([chain_tree(T) for _ in range(B)])
+    else:
+        parents = np.stack([random_tree(s_struct, T, cfg.max_depth, cfg.max_branch) for _ in range(B)])
+
+    q_bits = normal_bf16(s_vals, (B, T, H, D_QK))
+    kv_prefix = [normal_bf16(s_vals, (int(prefix_len[b]), D_QK)) for b in range(B)]
+    kv_tree = normal_bf16(s_vals, (B, T, D_QK))
+
+    need = int(prefix_len.sum()) + B * T
+    if need > cfg.pool_slots - 1:
+        raise ValueError("pool too small for the requests")
+    stride = max(1, int(prefix_len.max()))
+    slot_idx = np.zeros((B, stride), dtype=np.int32)
+    tree_slot = np.zeros((B, T), dtype=np.int32)
+    if layout == "contiguous":
+        src = FreeListAllocator(cfg.pool_slots)
+    elif layout == "perm":
+        perm = s_slots.permutation(np.arange(1, cfg.pool_slots, dtype=np.int64))
+        src = FreeListAllocator(cfg.pool_slots)
+        src.segments = collections.deque([perm])
+    elif layout == "churn":
+        keep = max(need + need // 4, (cfg.pool_slots - 1) // 10)
+        src = churned_allocator(s_slots, cfg.pool_slots, keep_free=min(keep, cfg.pool_slots - 1))
+    else:
+        raise ValueError(f"unknown slot layout {layout!r}")
+    for b in range(B):
+        L = int(prefix_len[b])
+        slot_idx[b, :L] = src.alloc(L)
+        tree_slot[b] = src.alloc(T)
+
+    return Workload(name=cfg.name, batch=B, nodes=T, heads=H, pool_slots=cfg.pool_slots,
+                    sm_scale=1.0 / math.sqrt(192.0), prefix_len=prefix_len, slot_stride=stride,
+                    slot_idx=slot_idx, tree_parent=parents.astype(np.int32), tree_slot_idx=tree_slot,
+                    q_bits=q_bits, kv_prefix_bits=kv_prefix, kv_tree_bits=kv_tree)
+
+
+def to_device(w: Workload, device="cuda", poison: bool = True):
+    """Upload a workload: pool rows at their slots, unused slots NaN-poisoned (or zero).
+
+    Returns a dict of torch tensors shaped as the C ABI expects.
+    """
+    import torch
+
+    fill = BF16_NAN if poison else 0
+    pool = torch.full((w.pool_slots, D_QK), fill, dtype=torch.int16, device=device)
+    for b in range(w.batch):
+        L = int(w.prefix_len[b])
+        if L:
+            idx = torch.from_numpy(w.slot_idx[b, :L].astype(np.int64)).to(device)
+            pool[idx] = torch.from_numpy(w.kv_prefix_bits[b].view(np.int16)).to(device)
+        idx = torch.from_numpy(w.tree_slot_idx[b].astype(np.int64)).to(device)
+        pool[idx] = torch.from_numpy(w.kv_tree_bits[b].view(np.int16)).to(device)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return {
+        "q": t(w.q_bits.view(np.int16)).view(torch.bfloat16),
+        "kv_pool": pool.view(torch.bfloat16),
+        "slot_idx": t(w.slot_idx),
+        "prefix_len": t(w.prefix_len),
+        "tree_parent": t(w.tree_parent),
+        "tree_slot_idx": t(w.tree_slot_idx),
+    }
