@@ -1,0 +1,152 @@
+/*
+ * ddtree.h -- C ABI of the DDTree verify-attention library for one GB300 (sm_103a).
+ *
+ * Operation ("The Architecture Detective: Uncovering FlashMLA's Potential for
+ * Blackwell DDTree Verification", sections "The Message in Full" and "The
+ * Discovery: FlashMLA's Hidden Capabilities"; "The Art of Systematic
+ * Investigation", section "Input Knowledge Required to Understand This
+ * Message"): in speculative decoding with a draft tree, every tree node of a
+ * request is verified in one pass.  Each node's query attends to
+ *   (a) the request's whole shared prefix, read through a page_size=1 token-slot
+ *       table from a KV pool whose slots may be scattered, with no causal limit
+ *       among the queries, and
+ *   (b) among the tree nodes, only its ancestors and itself.
+ * The attention is MLA in absorbed form: one KV head whose rows are 576 bf16
+ * values (512 latent + 64 rope dims, 1152 bytes per slot); scores are
+ * sm_scale * q.k over all 576 dims, values are the first 512 dims of the same row.
+ *
+ * Conventions for every entry point:
+ *   - All buffers are caller-owned device memory unless stated otherwise.  The
+ *     library allocates nothing, keeps no state between calls and never
+ *     synchronises the stream (except ddtree_read_device_status, which says so).
+ *   - All work is enqueued on `stream`; a call returns without waiting for it.
+ *   - Host-side checks return a negative DDT_ERR_* code before anything is
+ *     enqueued.  Problems that only the device can see (a slot index outside the
+ *     pool, a parent entry that is not a valid earlier node, a prefix length out
+ *     of range) never fault: the offending key or link is left out of the
+ *     attention and a bit is OR-ed into a status word in the workspace, which
+ *     ddtree_read_device_status returns.  The status word is cleared at the start
+ *     of every call that takes the workspace.
+ *   - Device pointers must be 16-byte aligned; bf16 is IEEE bfloat16.
+ */
+#ifndef DDTREE_H_
+#define DDTREE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DDT_API __attribute__((visibility("default")))
+#else
+#define DDT_API
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* ddt_stream_t;
+
+/* Host-side return codes. */
+#define DDT_OK 0
+#define DDT_ERR_NULL (-1)      /* a required pointer is NULL */
+#define DDT_ERR_DIMS (-2)      /* unsupported sizes (see ddt_dims) */
+#define DDT_ERR_WORKSPACE (-3) /* workspace smaller than ddtree_verify_workspace_bytes() */
+#define DDT_ERR_ALIGN (-4)     /* a device pointer is not 16-byte aligned */
+#define DDT_ERR_LAUNCH (-5)    /* a kernel launch or CUDA runtime call failed */
+#define DDT_ERR_DEVICE (-6)    /* the current device is not an sm_103 GPU */
+
+/* Device status bits (ddtree_read_device_status). */
+#define DDT_STATUS_BAD_SLOT 1      /* a slot index outside [0, pool_slots): key left out */
+#define DDT_STATUS_BAD_PARENT 2    /* tree_parent[b][0] != -1 or tree_parent[b][i] not in [0, i): link ignored */
+#define DDT_STATUS_BAD_PREFIX 4    /* prefix_len[b] outside [0, max_prefix_len]: clamped */
+#define DDT_STATUS_TIMEOUT 8       /* a bounded on-chip wait gave up; outputs are not valid */
+
+/*
+ * Sizes of one call.  Fixed by the library: D_qk = 576, D_v = 512.
+ *   batch          B >= 0 requests
+ *   num_nodes      T in [1, 128] tree nodes per request (node 0 is the root)
+ *   num_heads      H in [1, 1024] query heads (all share the single latent KV head)
+ *   pool_slots     N >= 1 rows in the KV pool
+ *   slot_stride    row stride (in entries) of slot_idx, >= max_prefix_len
+ *   max_prefix_len upper bound on every prefix_len[b]; it sizes the workspace
+ *                  and the launch.  The key-range split of each request depends
+ *                  only on this value, the device's SM count and prefix_len[b],
+ *                  never on slot addresses, so results are bitwise reproducible
+ *                  and identical for any slot layout of the same logical data.
+ */
+typedef struct {
+  int32_t batch;
+  int32_t num_nodes;
+  int32_t num_heads;
+  int32_t slot_stride;
+  int64_t pool_slots;
+  int32_t max_prefix_len;
+  int32_t reserved;
+} ddt_dims;
+
+/* Bytes of workspace ddtree_verify_attn needs for these sizes on the current
+ * device (0 if the sizes are unsupported).  Needs a current CUDA device. */
+DDT_API size_t ddtree_verify_workspace_bytes(const ddt_dims* dims);
+
+/*
+ * Verify attention for every (request b, node t, head h).
+ *
+ *   q             bf16 [B, T, H, 576], contiguous (row id (b*T + t)*H + h)
+ *   kv_pool       bf16 [N, 576], one latent row per slot
+ *   slot_idx      int32 [B, slot_stride]: request b's prefix position j lives in
+ *                 slot slot_idx[b*slot_stride + j], for j < prefix_len[b]
+ *   prefix_len    int32 [B], each in [0, max_prefix_len]
+ *   tree_parent   int32 [B, T]: parent[b][0] = -1, parent[b][i] in [0, i)
+ *                 (nodes in topological order)
+ *   tree_slot_idx int32 [B, T]: slot holding node i's own latent row
+ *   sm_scale      scale applied to q.k before the softmax
+ *   out           fp32 [B, T, H, 512] (written)
+ *   lse           fp32 [B, T, H] (written): natural log of the softmax normaliser
+ *   workspace     device scratch of >= ddtree_verify_workspace_bytes(dims) bytes,
+ *                 256-byte aligned; holds the per-split partial results and the
+ *                 status word.  Calls sharing a workspace must not overlap.
+ *
+ * Enqueues a prefix kernel (split-KV over each request's key range, all T*H rows
+ * of a request contracted together on the tensor cores) and a tail kernel (tree
+ * ancestors under the visibility rule, then the log-sum-exp merge of all parts).
+ * Capturable in a CUDA graph.  B = 0 enqueues nothing and returns DDT_OK.
+ */
+DDT_API int ddtree_verify_attn(const void* q, const void* kv_pool, const int32_t* slot_idx,
+                       const int32_t* prefix_len, const int32_t* tree_parent,
+                       const int32_t* tree_slot_idx, float sm_scale, float* out, float* lse,
+                       const ddt_dims* dims, void* workspace, size_t workspace_bytes,
+                       ddt_stream_t stream);
+
+/*
+ * KV compaction (defragmentation) of each request's prefix rows
+ * ("The Anatomy of a Kernel Investigation", section "The Reasoning Process: A
+ * Deep Dive", phase 3; "The Architecture Detective", section "Defragmentation:
+ * Separating Signal from Noise"):
+ *   kv_dst[dst_start[b] + j] = kv_src[slot_idx[b][j]]       (bit-exact row copy)
+ *   slot_idx_out[b][j]       = dst_start[b] + j
+ * for j < prefix_len[b].  Entries of slot_idx_out beyond prefix_len[b] are not
+ * written.  kv_src and kv_dst both have dims->pool_slots rows and may be the
+ * same pool only if no destination row [dst_start[b], dst_start[b]+prefix_len[b])
+ * is a source row of any request (the caller's contract; not checked).
+ *   dst_start   int64 [B] device
+ *   workspace   >= 256 bytes, 256-byte aligned (status word; bad source or
+ *               destination slots set DDT_STATUS_BAD_SLOT and skip the row)
+ */
+DDT_API int ddtree_kv_compact(const void* kv_src, void* kv_dst, const int32_t* slot_idx,
+                      const int32_t* prefix_len, const int64_t* dst_start, int32_t* slot_idx_out,
+                      const ddt_dims* dims, void* workspace, ddt_stream_t stream);
+
+/* Waits for `stream`, then copies the status word of the last call that used
+ * `workspace` to *host_status.  Returns DDT_OK or DDT_ERR_*. */
+DDT_API int ddtree_read_device_status(const void* workspace, int32_t* host_status, ddt_stream_t stream);
+
+/* Static text for a DDT_ERR_* return code. */
+DDT_API const char* ddtree_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DDTREE_H_ */

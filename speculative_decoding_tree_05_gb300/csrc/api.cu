@@ -1,0 +1,226 @@
+// api.cu -- the extern "C" boundary: argument checks, workspace plan, launches.
+#include <cuda_runtime.h>
+#include <mutex>
+#include "../../include/ddtree.h"
+#include "kernels.cuh"
+
+namespace ddt {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kStatusBytes = 256;
+
+struct DeviceInfo {
+  int sm_count = 0;
+  bool ok = false;      // sm_103 and kernels configured
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+// Per-device, once: check the architecture and opt the kernels into large
+// shared memory on that device.
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DDT_ERR_DEVICE;
+  std::call_once(g_once[dev], [dev] {
+    DeviceInfo d;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        major == 10 && minor == 3 && configure_prefix() == cudaSuccess && configure_tail_merge() == cudaSuccess)
+      d.ok = true;
+    g_dev[dev] = d;
+  });
+  *out = g_dev[dev];
+  return out->ok ? DDT_OK : DDT_ERR_DEVICE;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Plan {
+  int rows = 0, row_tiles = 0, chunk = kKeysPerTile, splits = 0;
+  size_t lse_off = 0, o_off = 0, bytes = 0;
+};
+
+int check_dims(const ddt_dims* d) {
+  if (!d) return DDT_ERR_NULL;
+  if (d->batch < 0 || d->num_nodes < 1 || d->num_nodes > kMaxNodes || d->num_heads < 1 || d->num_heads > 1024 ||
+      d->pool_slots < 1 || d->pool_slots > (int64_t(1) << 31) || d->max_prefix_len < 0 ||
+      d->slot_stride < d->max_prefix_len || d->slot_stride < 0)
+    return DDT_ERR_DIMS;
+  return DDT_OK;
+}
+
+// Key-range split of the prefix.  Depends only on the sizes and the SM count, so
+// a repeated call (or a call on a compacted pool) splits identically.
+int make_plan(const ddt_dims* d, int sm_count, Plan* plan) {
+  int rc = check_dims(d);
+  if (rc != DDT_OK) return rc;
+  Plan p;
+  p.rows = d->num_nodes * d->num_heads;
+  p.row_tiles = (p.rows + kTileRows - 1) / kTileRows;
+  const int64_t L = d->max_prefix_len;
+  if (L > 0 && d->batch > 0) {
+    const int64_t ctas_per_split = int64_t(d->batch) * p.row_tiles * 2;
+    const int64_t target = 2 * int64_t(sm_count);
+    int64_t splits = (target + ctas_per_split - 1) / ctas_per_split;
+    const int64_t max_tiles = (L + kKeysPerTile - 1) / kKeysPerTile;
+    if (splits > max_tiles) splits = max_tiles;
+    if (splits < 1) splits = 1;
+    int64_t chunk = (L + splits - 1) / splits;
+    chunk = (chunk + kKeysPerTile - 1) / kKeysPerTile * kKeysPerTile;
+    p.chunk = static_cast<int>(chunk);
+    p.splits = static_cast<int>((L + chunk - 1) / chunk);
+  }
+  const size_t part_rows = size_t(d->batch) * p.splits * p.row_tiles * kTileRows;
+  p.lse_off = kStatusBytes;
+  p.o_off = align_up(p.lse_off + part_rows * sizeof(float), 256);
+  p.bytes = p.o_off + part_rows * kDv * sizeof(float);
+  *plan = p;
+  return DDT_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace ddt
+
+using namespace ddt;
+
+extern "C" size_t ddtree_verify_workspace_bytes(const ddt_dims* dims) {
+  DeviceInfo dev;
+  if (device_info(&dev) != DDT_OK) return 0;
+  Plan plan;
+  if (make_plan(dims, dev.sm_count, &plan) != DDT_OK) return 0;
+  return plan.bytes;
+}
+
+extern "C" int ddtree_verify_attn(const void* q, const void* kv_pool, const int32_t* slot_idx,
+                                  const int32_t* prefix_len, const int32_t* tree_parent,
+                                  const int32_t* tree_slot_idx, float sm_scale, float* out, float* lse,
+                                  const ddt_dims* dims, void* workspace, size_t workspace_bytes,
+                                  ddt_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != DDT_OK) return rc;
+  if (dims->batch == 0) return DDT_OK;
+  if (!q || !kv_pool || !prefix_len || !tree_parent || !tree_slot_idx || !out || !lse || !workspace ||
+      (!slot_idx && dims->max_prefix_len > 0))
+    return DDT_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(workspace, 256) || !aligned(slot_idx, 4) || !aligned(prefix_len, 4) ||
+      !aligned(tree_parent, 4) || !aligned(tree_slot_idx, 4))
+    return DDT_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = device_info(&dev)) != DDT_OK) return rc;
+  Plan plan;
+  if ((rc = make_plan(dims, dev.sm_count, &plan)) != DDT_OK) return rc;
+  if (workspace_bytes < plan.bytes) return DDT_ERR_WORKSPACE;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
+
+  const float scale_log2 = sm_scale * 1.4426950408889634f;
+  float* lse_part = reinterpret_cast<float*>(ws + plan.lse_off);
+  float* o_part = reinterpret_cast<float*>(ws + plan.o_off);
+
+  if (plan.splits > 0) {
+    PrefixParams pp;
+    pp.q = static_cast<const uint16_t*>(q);
+    pp.kv = static_cast<const uint16_t*>(kv_pool);
+    pp.slot_idx = slot_idx;
+    pp.prefix_len = prefix_len;
+    pp.pool_slots = dims->pool_slots;
+    pp.slot_stride = dims->slot_stride;
+    pp.rows = plan.rows;
+    pp.row_tiles = plan.row_tiles;
+    pp.chunk = plan.chunk;
+    pp.max_splits = plan.splits;
+    pp.max_prefix_len = dims->max_prefix_len;
+    pp.scale_log2 = scale_log2;
+    pp.o_part = o_part;
+    pp.lse_part = lse_part;
+    pp.status = status;
+    if (launch_prefix(pp, dims->batch, plan.splits, s) != cudaSuccess) return DDT_ERR_LAUNCH;
+  }
+
+  TailParams tp;
+  tp.q = static_cast<const uint16_t*>(q);
+  tp.kv = static_cast<const uint16_t*>(kv_pool);
+  tp.prefix_len = prefix_len;
+  tp.tree_parent = tree_parent;
+  tp.tree_slot_idx = tree_slot_idx;
+  tp.pool_slots = dims->pool_slots;
+  tp.nodes = dims->num_nodes;
+  tp.heads = dims->num_heads;
+  tp.heads_per_cta = dims->num_heads < 16 ? dims->num_heads : 16;
+  tp.row_tiles = plan.row_tiles;
+  tp.chunk = plan.chunk;
+  tp.max_splits = plan.splits;
+  tp.max_prefix_len = dims->max_prefix_len;
+  tp.scale_log2 = scale_log2;
+  tp.o_part = o_part;
+  tp.lse_part = lse_part;
+  tp.out = out;
+  tp.lse = lse;
+  tp.status = status;
+  if (launch_tail_merge(tp, dims->batch, s) != cudaSuccess) return DDT_ERR_LAUNCH;
+  return DDT_OK;
+}
+
+extern "C" int ddtree_kv_compact(const void* kv_src, void* kv_dst, const int32_t* slot_idx,
+                                 const int32_t* prefix_len, const int64_t* dst_start, int32_t* slot_idx_out,
+                                 const ddt_dims* dims, void* workspace, ddt_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != DDT_OK) return rc;
+  if (dims->batch == 0) return DDT_OK;
+  if (!kv_src || !kv_dst || !prefix_len || !dst_start || !workspace ||
+      ((!slot_idx || !slot_idx_out) && dims->max_prefix_len > 0))
+    return DDT_ERR_NULL;
+  if (!aligned(kv_src, 16) || !aligned(kv_dst, 16) || !aligned(workspace, 256) || !aligned(dst_start, 8) ||
+      !aligned(slot_idx, 4) || !aligned(slot_idx_out, 4) || !aligned(prefix_len, 4))
+    return DDT_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = device_info(&dev)) != DDT_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* status = static_cast<int32_t*>(workspace);
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
+  CompactParams cp;
+  cp.src = static_cast<const uint16_t*>(kv_src);
+  cp.dst = static_cast<uint16_t*>(kv_dst);
+  cp.slot_idx = slot_idx;
+  cp.prefix_len = prefix_len;
+  cp.dst_start = dst_start;
+  cp.slot_idx_out = slot_idx_out;
+  cp.pool_slots = dims->pool_slots;
+  cp.slot_stride = dims->slot_stride;
+  cp.max_prefix_len = dims->max_prefix_len;
+  cp.status = status;
+  if (launch_kv_compact(cp, dims->batch, s) != cudaSuccess) return DDT_ERR_LAUNCH;
+  return DDT_OK;
+}
+
+extern "C" int ddtree_read_device_status(const void* workspace, int32_t* host_status, ddt_stream_t stream) {
+  if (!workspace || !host_status) return DDT_ERR_NULL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DDT_ERR_LAUNCH;
+  if (cudaMemcpy(host_status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DDT_ERR_LAUNCH;
+  return DDT_OK;
+}
+
+extern "C" const char* ddtree_status_string(int code) {
+  switch (code) {
+    case DDT_OK: return "ok";
+    case DDT_ERR_NULL: return "a required pointer is NULL";
+    case DDT_ERR_DIMS: return "unsupported sizes";
+    case DDT_ERR_WORKSPACE: return "workspace too small";
+    case DDT_ERR_ALIGN: return "a device pointer is misaligned";
+    case DDT_ERR_LAUNCH: return "a kernel launch or CUDA runtime call failed";
+    case DDT_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    default: return "unknown status";
+  }
+}

@@ -1,0 +1,91 @@
+// kernels.cuh -- launch parameters shared by the host launcher and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ddt {
+
+constexpr int kDqk = 576;       // q/k width: 512 latent + 64 rope
+constexpr int kDv = 512;        // v width: latent part of the same row
+constexpr int kRowBytes = kDqk * 2;
+constexpr int kChunks = kRowBytes / 16;   // 72 x 16-byte chunks per latent row
+constexpr int kMaxNodes = 128;
+
+constexpr int32_t kStatusBadSlot = 1;
+constexpr int32_t kStatusBadParent = 2;
+constexpr int32_t kStatusBadPrefix = 4;
+constexpr int32_t kStatusTimeout = 8;
+
+// Split-KV prefix pass: one CTA per (request, 128-row tile, v-half, key split).
+struct PrefixParams {
+  const uint16_t* q;         // bf16 [B, T, H, 576]
+  const uint16_t* kv;        // bf16 [N, 576]
+  const int32_t* slot_idx;   // [B, slot_stride]
+  const int32_t* prefix_len; // [B]
+  int64_t pool_slots;
+  int32_t slot_stride;
+  int32_t rows;              // T * H rows per request
+  int32_t row_tiles;         // ceil(rows / 128)
+  int32_t chunk;             // keys per split
+  int32_t max_splits;        // split slots per request in the workspace
+  int32_t max_prefix_len;
+  float scale_log2;          // sm_scale * log2(e)
+  float* o_part;             // fp32 [B, max_splits, row_tiles*128, 512]
+  float* lse_part;           // fp32 [B, max_splits, row_tiles*128], natural log
+  int32_t* status;
+};
+
+// Tree tail + merge: one CTA per (request, node, head group).
+struct TailParams {
+  const uint16_t* q;
+  const uint16_t* kv;
+  const int32_t* prefix_len;
+  const int32_t* tree_parent;   // [B, T]
+  const int32_t* tree_slot_idx; // [B, T]
+  int64_t pool_slots;
+  int32_t nodes;                // T
+  int32_t heads;                // H
+  int32_t heads_per_cta;
+  int32_t row_tiles;
+  int32_t chunk;
+  int32_t max_splits;
+  int32_t max_prefix_len;
+  float scale_log2;
+  const float* o_part;
+  const float* lse_part;
+  float* out;                   // fp32 [B, T, H, 512]
+  float* lse;                   // fp32 [B, T, H]
+  int32_t* status;
+};
+
+struct CompactParams {
+  const uint16_t* src;
+  uint16_t* dst;
+  const int32_t* slot_idx;
+  const int32_t* prefix_len;
+  const int64_t* dst_start;
+  int32_t* slot_idx_out;
+  int64_t pool_slots;
+  int32_t slot_stride;
+  int32_t max_prefix_len;
+  int32_t* status;
+};
+
+// Prefix kernel geometry.
+constexpr int kTileRows = 128;            // query rows per CTA (tcgen05 M)
+constexpr int kKeysPerTile = 32;          // keys per pipeline step (S tile N)
+constexpr int kPrefixThreads = 128;
+constexpr int kQBytes = kTileRows * kRowBytes;           // 147456
+constexpr int kKTileBytes = kKeysPerTile * kRowBytes;    // 36864
+constexpr int kPBytes = kTileRows * kKeysPerTile * 2;    // 8192
+constexpr int kPrefixSmem = kQBytes + 2 * kKTileBytes + kPBytes + 1024;
+
+// Per-device set-up (shared-memory opt-in), called once per device before launches.
+cudaError_t configure_prefix();
+cudaError_t configure_tail_merge();
+
+cudaError_t launch_prefix(const PrefixParams& p, int batch, int splits, cudaStream_t stream);
+cudaError_t launch_tail_merge(const TailParams& p, int batch, cudaStream_t stream);
+cudaError_t launch_kv_compact(const CompactParams& p, int batch, cudaStream_t stream);
+
+}  // namespace ddt

@@ -1,0 +1,178 @@
+// tail_merge.cu -- tree-tail attention under the ancestor mask, then the
+// log-sum-exp merge of every partial result of a row.
+//
+// Among the tree nodes a draft node sees only its ancestors and itself ("The Art
+// of Systematic Investigation", section "Input Knowledge Required to Understand
+// This Message", item 1).  That part is tiny (at most T keys per row), so it runs
+// on the CUDA cores next to the merge instead of in the tensor-core pass
+// ("The Architecture Detective: Uncovering FlashMLA's Potential for Blackwell
+// DDTree Verification", section "The Message in Full": a small custom kernel for
+// the masked tree tail, merged with the prefix result through the softmax
+// state; "The Anatomy of a Kernel Investigation", section "The Reasoning
+// Process: A Deep Dive", phase 2).
+//
+// One CTA = (request b, node t, group of heads).  Thread 0 walks the parent
+// chain of t (validating each link), the CTA stages the visible tree rows in
+// shared memory, then each warp takes one head row at a time:
+//   tail:  s_u = scale * q.k_u for the visible u, online softmax, o_t = sum p_u v_u
+//   merge: lse = log2-sum-exp over {tail, prefix splits}, out = weighted sum of
+//          the normalised partial outputs; lse is reported in natural log.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace ddt {
+namespace {
+
+constexpr int kTailThreads = 256;
+constexpr int kTailWarps = kTailThreads / 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) {
+  extern __shared__ __align__(16) uint8_t rows_sh[];  // visible tree rows, 1152 B each
+  __shared__ int n_vis_sh;
+  __shared__ int vis_slot_sh[kMaxNodes];
+
+  const int t = blockIdx.x;
+  const int b = blockIdx.z;
+  const int T = p.nodes;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  if (tid == 0) {
+    int n = 0, u = t;
+    const int32_t* par = p.tree_parent + static_cast<int64_t>(b) * T;
+    const int32_t* tsl = p.tree_slot_idx + static_cast<int64_t>(b) * T;
+    int32_t st = 0;
+    for (int guard = 0; u >= 0 && guard < T; ++guard) {
+      int32_t slot = tsl[u];
+      if (slot >= 0 && static_cast<int64_t>(slot) < p.pool_slots)
+        vis_slot_sh[n++] = slot;
+      else
+        st |= kStatusBadSlot;
+      int pu = par[u];
+      bool ok = (u == 0) ? (pu == -1) : (pu >= 0 && pu < u);
+      if (!ok) {
+        st |= kStatusBadParent;
+        break;
+      }
+      u = pu;
+    }
+    n_vis_sh = n;
+    if (st && blockIdx.y == 0) atomicOr(p.status, st);
+  }
+  __syncthreads();
+  const int n_vis = n_vis_sh;
+  for (int i = tid; i < n_vis * kChunks; i += kTailThreads) {
+    int v = i / kChunks, c = i - v * kChunks;
+    const uint4* src = reinterpret_cast<const uint4*>(p.kv + static_cast<int64_t>(vis_slot_sh[v]) * kDqk) + c;
+    reinterpret_cast<uint4*>(rows_sh + v * kRowBytes)[c] = __ldg(src);
+  }
+  __syncthreads();
+
+  int L = __ldg(p.prefix_len + b);
+  L = L < 0 ? 0 : (L > p.max_prefix_len ? p.max_prefix_len : L);
+  const int splits = (L + p.chunk - 1) / p.chunk;
+  const int h0 = blockIdx.y * p.heads_per_cta;
+  const int h1 = min(p.heads, h0 + p.heads_per_cta);
+
+  for (int h = h0 + warp; h < h1; h += kTailWarps) {
+    const int r = t * p.heads + h;                                // row within the request
+    const int64_t grow = static_cast<int64_t>(b) * T * p.heads + r;  // global row
+    // q: lane holds dims {64 i + 2 lane, +1}, i = 0..8
+    uint32_t qv[9];
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + grow * kDqk);
+#pragma unroll
+    for (int i = 0; i < 9; ++i) qv[i] = __ldg(qrow + 32 * i + lane);
+
+    // tail: online softmax over the visible tree rows, log2 domain
+    float m = -CUDART_INF_F, l = 0.f, o[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j] = 0.f;
+    for (int v = 0; v < n_vis; ++v) {
+      const uint32_t* krow = reinterpret_cast<const uint32_t*>(rows_sh + v * kRowBytes);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 9; ++i) {
+        uint32_t kk = krow[32 * i + lane];
+        acc = fmaf(bf16_lo(qv[i]), bf16_lo(kk), acc);
+        acc = fmaf(bf16_hi(qv[i]), bf16_hi(kk), acc);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const float s = acc * p.scale_log2;
+      const float mn = fmaxf(m, s);
+      const float alpha = fast_exp2(m - mn);
+      const float pv = fast_exp2(s - mn);
+      l = l * alpha + pv;
+      m = mn;
+      // v dims of this lane: 4 lane + 128 j + {0..3}, j = 0..3
+      const uint2* vrow = reinterpret_cast<const uint2*>(rows_sh + v * kRowBytes);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint2 w = vrow[lane + 32 * j];
+        o[4 * j + 0] = fmaf(o[4 * j + 0], alpha, pv * bf16_lo(w.x));
+        o[4 * j + 1] = fmaf(o[4 * j + 1], alpha, pv * bf16_hi(w.x));
+        o[4 * j + 2] = fmaf(o[4 * j + 2], alpha, pv * bf16_lo(w.y));
+        o[4 * j + 3] = fmaf(o[4 * j + 3], alpha, pv * bf16_hi(w.y));
+      }
+    }
+    // parts: tail (lse2_t, o / l) and every prefix split (lse_s, o_s normalised)
+    const float lse2_t = (l > 0.f) ? m + log2f(l) : -CUDART_INF_F;
+    float mx = lse2_t;
+    const int64_t pstride = static_cast<int64_t>(p.row_tiles) * kTileRows;
+    const int64_t pbase = static_cast<int64_t>(b) * p.max_splits * pstride + r;
+    for (int s = 0; s < splits; ++s) mx = fmaxf(mx, __ldg(p.lse_part + pbase + s * pstride) * kLog2e);
+
+    float acc[16];
+    float wsum = 0.f;
+    if (mx == -CUDART_INF_F) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    } else {
+      const float wt = (l > 0.f) ? fast_exp2(lse2_t - mx) : 0.f;
+      const float wt_l = (l > 0.f) ? wt / l : 0.f;
+      wsum = wt;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = o[j] * wt_l;
+      for (int s = 0; s < splits; ++s) {
+        const float ws = fast_exp2(__ldg(p.lse_part + pbase + s * pstride) * kLog2e - mx);
+        wsum += ws;
+        const float4* op = reinterpret_cast<const float4*>(p.o_part + (pbase + s * pstride) * kDv);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float4 x = __ldg(op + lane + 32 * j);
+          acc[4 * j + 0] = fmaf(ws, x.x, acc[4 * j + 0]);
+          acc[4 * j + 1] = fmaf(ws, x.y, acc[4 * j + 1]);
+          acc[4 * j + 2] = fmaf(ws, x.z, acc[4 * j + 2]);
+          acc[4 * j + 3] = fmaf(ws, x.w, acc[4 * j + 3]);
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    float4* dst = reinterpret_cast<float4*>(p.out + grow * kDv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      dst[lane + 32 * j] = make_float4(acc[4 * j] * inv, acc[4 * j + 1] * inv, acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
+    if (lane == 0) p.lse[grow] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -CUDART_INF_F;
+  }
+}
+
+}  // namespace
+
+cudaError_t configure_tail_merge() {
+  return cudaFuncSetAttribute(tail_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxNodes * kRowBytes);
+}
+
+cudaError_t launch_tail_merge(const TailParams& p, int batch, cudaStream_t stream) {
+  const int smem = p.nodes * kRowBytes;
+  dim3 grid(p.nodes, (p.heads + p.heads_per_cta - 1) / p.heads_per_cta, batch);
+  tail_merge_kernel<<<grid, kTailThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ddt

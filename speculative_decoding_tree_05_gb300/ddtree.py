@@ -1,0 +1,160 @@
+"""Thin ctypes binding of include/ddtree.h: argument marshalling only.
+
+Every step of the computation runs in the CUDA library (lib/libddtree.so).
+PyTorch only provides device memory and the current stream.  If the library is
+missing this module raises at import-time use; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libddtree.so")
+
+D_QK = 576
+D_V = 512
+
+DDT_OK = 0
+ERRORS = {-1: "DDT_ERR_NULL", -2: "DDT_ERR_DIMS", -3: "DDT_ERR_WORKSPACE", -4: "DDT_ERR_ALIGN",
+          -5: "DDT_ERR_LAUNCH", -6: "DDT_ERR_DEVICE"}
+STATUS_BAD_SLOT = 1
+STATUS_BAD_PARENT = 2
+STATUS_BAD_PREFIX = 4
+STATUS_TIMEOUT = 8
+
+EXPORTS = ("ddtree_verify_workspace_bytes", "ddtree_verify_attn", "ddtree_kv_compact",
+           "ddtree_read_device_status", "ddtree_status_string")
+
+
+class DDTError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({status_string(code)})")
+        self.code = code
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_nodes", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("slot_stride", ctypes.c_int32), ("pool_slots", ctypes.c_int64),
+                ("max_prefix_len", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    """Load lib/libddtree.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing (run __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32p = ctypes.c_void_p, ctypes.c_void_p
+        L.ddtree_verify_workspace_bytes.restype = ctypes.c_size_t
+        L.ddtree_verify_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+        L.ddtree_verify_attn.restype = ctypes.c_int
+        L.ddtree_verify_attn.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp,
+                                         ctypes.POINTER(Dims), vp, ctypes.c_size_t, vp]
+        L.ddtree_kv_compact.restype = ctypes.c_int
+        L.ddtree_kv_compact.argtypes = [vp, vp, i32p, i32p, vp, i32p, ctypes.POINTER(Dims), vp, vp]
+        L.ddtree_read_device_status.restype = ctypes.c_int
+        L.ddtree_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+        L.ddtree_status_string.restype = ctypes.c_char_p
+        L.ddtree_status_string.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().ddtree_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_dims(batch, nodes, heads, pool_slots, slot_stride, max_prefix_len) -> Dims:
+    return Dims(int(batch), int(nodes), int(heads), int(slot_stride), int(pool_slots), int(max_prefix_len), 0)
+
+
+def workspace_bytes(dims: Dims) -> int:
+    return int(lib().ddtree_verify_workspace_bytes(ctypes.byref(dims)))
+
+
+def _check(rc, what):
+    if rc != DDT_OK:
+        raise DDTError(rc, what)
+
+
+class Verifier:
+    """Holds a workspace sized for one set of dims and runs verify calls with it.
+
+    q [B,T,H,576] bf16, kv_pool [N,576] bf16, slot_idx [B,stride] int32, prefix_len [B] int32,
+    tree_parent [B,T] int32, tree_slot_idx [B,T] int32 -- all CUDA tensors.
+    """
+
+    def __init__(self, batch, nodes, heads, pool_slots, slot_stride, max_prefix_len=None, device=None):
+        import torch
+        self.dims = make_dims(batch, nodes, heads, pool_slots, slot_stride,
+                              slot_stride if max_prefix_len is None else max_prefix_len)
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        with torch.cuda.device(self.device):
+            n = workspace_bytes(self.dims)
+            if n == 0:
+                raise DDTError(-2, "ddtree_verify_workspace_bytes")
+            self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device)
+
+    def __call__(self, q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out=None,
+                 lse=None, stream=None):
+        import torch
+        B, T, H, D = q.shape
+        if out is None:
+            out = torch.empty((B, T, H, D_V), dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+        rc = lib().ddtree_verify_attn(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len), _ptr(tree_parent),
+                                      _ptr(tree_slot_idx), float(sm_scale), _ptr(out), _ptr(lse),
+                                      ctypes.byref(self.dims), _ptr(self.workspace), self.workspace.numel(),
+                                      _stream(stream))
+        _check(rc, "ddtree_verify_attn")
+        return out, lse
+
+    def status(self, stream=None) -> int:
+        return read_device_status(self.workspace, stream)
+
+
+def verify_attn(q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, max_prefix_len=None,
+                out=None, lse=None, stream=None):
+    """One-off verify call (allocates its own workspace); returns (out, lse)."""
+    B, T, H, _ = q.shape
+    v = Verifier(B, T, H, kv_pool.shape[0], slot_idx.shape[1], max_prefix_len, device=q.device)
+    return v(q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out, lse, stream)
+
+
+def kv_compact(kv_src, kv_dst, slot_idx, prefix_len, dst_start, slot_idx_out=None, max_prefix_len=None,
+               workspace=None, stream=None):
+    """Copy each request's prefix rows to dst_start[b] + j; returns slot_idx_out."""
+    import torch
+    B, stride = slot_idx.shape
+    if slot_idx_out is None:
+        slot_idx_out = slot_idx.clone()
+    if workspace is None:
+        workspace = torch.empty(256, dtype=torch.uint8, device=slot_idx.device)
+    dims = make_dims(B, 1, 1, kv_src.shape[0], stride, stride if max_prefix_len is None else max_prefix_len)
+    rc = lib().ddtree_kv_compact(_ptr(kv_src), _ptr(kv_dst), _ptr(slot_idx), _ptr(prefix_len), _ptr(dst_start),
+                                 _ptr(slot_idx_out), ctypes.byref(dims), _ptr(workspace), _stream(stream))
+    _check(rc, "ddtree_kv_compact")
+    return slot_idx_out
+
+
+def read_device_status(workspace, stream=None) -> int:
+    st = ctypes.c_int32(0)
+    rc = lib().ddtree_read_device_status(_ptr(workspace), ctypes.byref(st), _stream(stream))
+    _check(rc, "ddtree_read_device_status")
+    return int(st.value)

@@ -38,7 +38,7 @@ BF16_NAN = 0x7FC0   # quiet NaN used to poison slots no request owns
 class Config:
     name: str
     batch: int
-    prefix: tuple            # fixed prefix length per request, or ("uniform", lo, hi)
+    prefix: tuple            # (L,) for every request, ("uniform", lo, hi) or ("list", L0, L1, ...)
     nodes: int               # tree nodes per request (node 0 is the root)
     tree: str                # "random" or "chain"
     max_depth: int
@@ -143,6 +143,8 @@ class FreeListAllocator:
         self.free_count = pool_slots - 1
 
     def alloc(self, n: int) -> np.ndarray:
+        if n == 0:
+            return np.zeros(0, dtype=np.int64)
         if n > self.free_count:
             raise MemoryError(f"alloc({n}) with {self.free_count} free slots")
         parts, need = [], n
@@ -267,6 +269,8 @@ def _prefix_lengths(cfg: Config, rng: np.random.Generator) -> np.ndarray:
     if cfg.prefix[0] == "uniform":
         _, lo, hi = cfg.prefix
         return rng.integers(lo, hi + 1, size=cfg.batch).astype(np.int32)
+    if cfg.prefix[0] == "list":
+        return np.asarray(cfg.prefix[1:], dtype=np.int32)
     return np.full(cfg.batch, int(cfg.prefix[0]), dtype=np.int32)
 
 

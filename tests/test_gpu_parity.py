@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerances (bf16 inputs, fp32 accumulation): out max-abs <= 2e-2 and
+mean-abs <= 2e-3, lse abs <= 1e-3.  Small cases compare every element; the
+full-size configurations compare sampled rows the oracle computes one by one
+(rows spread over every 128-row tile, including the ragged last tile) and check
+properties that hold at any size (finite outputs, determinism, layout
+invariance, bit-exact compaction).  Unused pool slots hold NaN, so a gather
+from a wrong slot shows up as NaN.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_tree_05_gb300 import ddtree, workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+OUT_MAX, OUT_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_tree_05_gb300 import build
+    build.build()
+    ddtree.lib()
+
+
+def run_gpu(w, poison=True, dev=None):
+    d = wl.to_device(w, "cuda", poison=poison) if dev is None else dev
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len)
+    out, lse = v(d["q"], d["kv_pool"], d["slot_idx"], d["prefix_len"], d["tree_parent"], d["tree_slot_idx"],
+                 w.sm_scale)
+    status = v.status()
+    return out, lse, status, d
+
+
+def sample_rows(w, n_per_tile=3, seed=0):
+    """Rows of every request: a few per 128-row tile, plus first and last row."""
+    rng = np.random.default_rng(seed)
+    R = w.rows_per_request
+    rows = []
+    for b in range(w.batch):
+        base = b * R
+        for t0 in range(0, R, 128):
+            t1 = min(R, t0 + 128)
+            rows.extend(base + rng.choice(np.arange(t0, t1), size=min(n_per_tile, t1 - t0), replace=False))
+        rows.extend([base, base + R - 1])
+    return np.unique(np.asarray(rows, np.int64))
+
+
+def compare(out, lse, ref_o, ref_l, rows=None):
+    o = out.reshape(-1, wl.D_V).cpu().numpy().astype(np.float64)
+    l = lse.reshape(-1).cpu().numpy().astype(np.float64)
+    if rows is not None:
+        o, l = o[rows], l[rows]
+    ref_o = ref_o.reshape(-1, wl.D_V)
+    ref_l = ref_l.reshape(-1)
+    assert np.isfinite(o).all() and np.isfinite(l).all()
+    e_o = np.abs(o - ref_o)
+    e_l = np.abs(l - ref_l)
+    msg = f"out max {e_o.max():.3e} mean {e_o.mean():.3e} lse max {e_l.max():.3e}"
+    assert e_o.max() <= OUT_MAX and e_o.mean() <= OUT_MEAN and e_l.max() <= LSE_MAX, msg
+    return e_o.max(), e_o.mean(), e_l.max()
+
+
+# ----------------------------------------------------------------------------- small cases, every element
+
+def test_tiny_full():
+    w = wl.make_workload("tiny")
+    out, lse, st, _ = run_gpu(w)
+    assert st == 0
+    ref_o, ref_l, _ = oracle.verify_workload(w)
+    compare(out, lse, ref_o, ref_l)
+
+
+def test_c2_full():
+    w = wl.make_workload("c2")
+    out, lse, st, _ = run_gpu(w)
+    assert st == 0
+    ref_o, ref_l, _ = oracle.verify_workload(w)
+    compare(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("prefix,nodes,heads,tree", [
+    ((0,), 9, 16, "random"),          # tree only
+    ((1,), 1, 1, "chain"),            # single key + single node
+    ((31,), 5, 3, "random"),          # ragged below one key step
+    ((33,), 65, 2, "random"),         # one step + 1 key; 130 rows -> ragged second tile
+    ((1000,), 128, 1, "random"),      # maximum node count
+    ((517, 0, 64), 7, 20, "chain"),   # ragged batch incl. an empty prefix
+    ((3000,), 17, 8, "random"),       # 136 rows: tile of 128 + 8
+])
+def test_edge_cases(prefix, nodes, heads, tree):
+    w = wl.make_workload("tiny", batch=len(prefix), prefix=("list", *prefix), nodes=nodes, heads=heads, tree=tree,
+                         max_depth=8, max_branch=0, pool_slots=1 << 16, slots="churn")
+    out, lse, st, _ = run_gpu(w)
+    assert st == 0
+    ref_o, ref_l, _ = oracle.verify_workload(w)
+    compare(out, lse, ref_o, ref_l)
+
+
+def test_deterministic_and_layout_invariant():
+    w = wl.make_workload("tiny", prefix=(4099,), nodes=33, heads=16, max_depth=6, max_branch=4)
+    o1, l1, _, d = run_gpu(w)
+    o2, l2, _, _ = run_gpu(w, dev=d)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    wc = wl.make_workload("tiny", prefix=(4099,), nodes=33, heads=16, max_depth=6, max_branch=4, slots="contiguous")
+    o3, l3, _, _ = run_gpu(wc)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+# ----------------------------------------------------------------------------- device-side validation
+
+def test_bad_slot_is_masked_and_reported():
+    w = wl.make_workload("tiny", prefix=(300,))
+    w.slot_idx[0, 77] = w.pool_slots + 12
+    w.tree_slot_idx[0, 3] = -5
+    d = wl.to_device(w, "cuda")
+    out, lse, st, _ = run_gpu(w, dev=d)
+    assert st & ddtree.STATUS_BAD_SLOT
+    pool, si, ts = w.compact_host_pool()
+    si[0, 77] = pool.shape[0] + 12     # the oracle leaves the same keys out
+    ts[0, 3] = -5
+    ref_o, ref_l, ost = oracle.verify_attn(w.q_bits, pool, si, w.prefix_len, w.tree_parent, ts, w.sm_scale)
+    assert ost & oracle.BAD_SLOT
+    compare(out, lse, ref_o, ref_l)
+
+
+def test_bad_parent_is_ignored_and_reported():
+    w = wl.make_workload("tiny")
+    w.tree_parent[0, 5] = 7            # forward link: not an earlier node
+    out, lse, st, _ = run_gpu(w)
+    assert st & ddtree.STATUS_BAD_PARENT
+    ref_o, ref_l, ost = oracle.verify_workload(w)
+    assert ost & oracle.BAD_PARENT
+    compare(out, lse, ref_o, ref_l)
+
+
+def test_prefix_len_above_bound_is_reported():
+    w = wl.make_workload("tiny")
+    d = wl.to_device(w, "cuda")
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, max_prefix_len=200)
+    v(d["q"], d["kv_pool"], d["slot_idx"], d["prefix_len"], d["tree_parent"], d["tree_slot_idx"], w.sm_scale)
+    assert v.status() & ddtree.STATUS_BAD_PREFIX
+
+
+def test_host_errors_on_gpu():
+    w = wl.make_workload("tiny")
+    d = wl.to_device(w, "cuda")
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride)
+    small = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride)
+    small.workspace = small.workspace[:100]
+    with pytest.raises(ddtree.DDTError) as e:
+        small(d["q"], d["kv_pool"], d["slot_idx"], d["prefix_len"], d["tree_parent"], d["tree_slot_idx"], 0.1)
+    assert e.value.code == -3
+    assert ddtree.workspace_bytes(v.dims) > 0
+
+
+# ----------------------------------------------------------------------------- full-size configurations
+
+@pytest.mark.parametrize("name", ["c3", "c4", "c5"])
+def test_full_size_sampled(name):
+    w = wl.make_workload(name)
+    out, lse, st, d = run_gpu(w)
+    assert st == 0
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    rows = sample_rows(w, n_per_tile=2 if name == "c3" else 4)
+    ref_o, ref_l, _ = oracle.verify_workload(w, rows=rows)
+    compare(out, lse, ref_o, ref_l, rows=rows)
+    if name == "c3":
+        # same logical data on contiguous slots: bitwise identical results
+        del d
+        wc = wl.make_workload(name, slots="contiguous")
+        oc, lc, stc, _ = run_gpu(wc)
+        assert stc == 0 and torch.equal(out, oc) and torch.equal(lse, lc)
+
+
+def test_c5_compaction_bit_exact():
+    w = wl.make_workload("c5")
+    d = wl.to_device(w, "cuda", poison=True)
+    out1, lse1, st, _ = run_gpu(w, dev=d)
+    assert st == 0
+    # destination: one contiguous run per request in a fresh pool
+    starts = np.concatenate([[1], 1 + np.cumsum(w.prefix_len[:-1].astype(np.int64))])
+    dst_pool = torch.full_like(d["kv_pool"].view(torch.int16), wl.BF16_NAN).view(torch.bfloat16)
+    ts = d["tree_slot_idx"].reshape(-1).long()
+    free_tail = int(starts[-1] + w.prefix_len[-1])
+    assert free_tail <= w.pool_slots
+    # the tree rows move above the compacted runs
+    new_tree = torch.arange(free_tail, free_tail + w.batch * w.nodes, dtype=torch.int32, device="cuda")
+    dst_pool[new_tree.long()] = d["kv_pool"][ts]
+    dst_start = torch.from_numpy(starts).cuda()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    new_idx = ddtree.kv_compact(d["kv_pool"], dst_pool, d["slot_idx"], d["prefix_len"], dst_start, workspace=ws)
+    assert ddtree.read_device_status(ws) == 0
+    for b in range(w.batch):
+        L = int(w.prefix_len[b])
+        s0 = int(starts[b])
+        assert torch.equal(new_idx[b, :L].cpu(), torch.arange(s0, s0 + L, dtype=torch.int32))
+        got = dst_pool[s0:s0 + L].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, w.kv_prefix_bits[b])
+    d2 = dict(d, kv_pool=dst_pool, slot_idx=new_idx, tree_slot_idx=new_tree.view(w.batch, w.nodes))
+    out2, lse2, st2, _ = run_gpu(w, dev=d2)
+    assert st2 == 0
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    rows = sample_rows(w, n_per_tile=2)
+    ref_o, ref_l, _ = oracle.verify_workload(w, rows=rows)
+    compare(out2, lse2, ref_o, ref_l, rows=rows)
