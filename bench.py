@@ -1,0 +1,333 @@
+"""Benchmark of DDTree verify attention (MLA 576/512) on GB300.
+
+One step = one ddtree_verify_attn call over the whole batch (prefix split-KV
+kernel + tree-tail/merge kernel), inputs resident in HBM.  L2 is flushed (a
+256 MiB write) before every timed step; the flush is outside the step's events.
+
+Prints ONE JSON line on rank 0.  value = effective KV GB/s over all ranks
+(every prefix and tree row of every request, 1152 B each, once per step,
+divided by the device time of the steps).  Under torchrun each rank runs an
+independent replica of the workload (weak scaling; no collective exists on
+this path).
+
+--impl reference times the fp64 CPU oracle (the only reference this project
+has) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_tree_05_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verify-attn µs/step and effective KV GB/s (fraction of GB300 roofline)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+PREFIX_SRC = os.path.join(ROOT, "speculative_decoding_tree_05_gb300", "csrc", "prefix_attn.cu")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per prefix-kernel launch from a committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(PROFILE_DIR, f"prefix_attn_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_src or not m_b or m_src.group(1) != source_digest(PREFIX_SRC):
+        return None
+    return float(m_b.group(1))
+
+
+def workload_config(w, name, layout):
+    return {"workload": f"{name}: {wl.DESCRIPTIONS[name]}", "batch": w.batch, "prefix_len_total": int(w.prefix_len.sum()),
+            "tree_nodes": w.nodes, "heads": w.heads, "d_qk": wl.D_QK, "d_v": wl.D_V, "pool_slots": w.pool_slots,
+            "slots": layout, "l2": "flushed before every step (256 MiB write)", "parallelism": "replicas"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample_rate(w, budget_s=8.0, min_rows=8):
+    """Time the fp64 oracle on growing row samples; returns (seconds per row, rows timed, threads)."""
+    import oracle
+    oracle.load()
+    total = w.batch * w.rows_per_request
+    rng = np.random.default_rng(1234)
+    order = rng.permutation(total)
+    done, spent, n = 0, 0.0, min_rows
+    while done < total and spent < budget_s:
+        rows = np.sort(order[done:done + n])
+        t0 = time.perf_counter()
+        oracle.verify_workload(w, rows=rows)
+        spent += time.perf_counter() - t0
+        done += len(rows)
+        n = min(total - done, n * 2)
+    threads = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    return spent / done, done, threads
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    name = args.config
+    w = wl.make_workload(name)
+    total = w.batch * w.rows_per_request
+    kv_bytes = w.kv_bytes()
+    import oracle
+    oracle.load()
+    rng = np.random.default_rng(77)
+    per_step_rows = max(1, min(total, args.ref_rows))
+    times = []
+    for step in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(total, size=per_step_rows, replace=False))
+        t0 = time.perf_counter()
+        oracle.verify_workload(w, rows=rows)
+        dt = (time.perf_counter() - t0) * total / per_step_rows   # scaled to the whole step
+        if step >= args.warmup:
+            times.append(dt)
+    step_s = statistics.mean(times)
+    value = kv_bytes / step_s / 1e9
+    cores = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    sample = f"{per_step_rows} of {total} rows per step, time scaled by rows to a full step"
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": workload_config(w, name, wl.CONFIGS[name].slots),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from speculative_decoding_tree_05_gb300 import ddtree
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    name = args.config
+    layout = args.slots or wl.CONFIGS[name].slots
+    w = wl.make_workload(name, slots=layout)
+    d = wl.to_device(w, dev, poison=False)
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len, device=dev)
+    out = torch.empty((w.batch, w.nodes, w.heads, wl.D_V), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.batch, w.nodes, w.heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    args_v = (d["q"], d["kv_pool"], d["slot_idx"], d["prefix_len"], d["tree_parent"], d["tree_slot_idx"], w.sm_scale)
+
+    def step(ev):
+        flush.fill_(1)                       # outside the step's events
+        ev[0].record(stream)
+        v(*args_v, out=out, lse=lse, phase="prefix")
+        ev[1].record(stream)
+        v(*args_v, out=out, lse=lse, phase="merge")
+        ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize(dev)
+    assert v.status() == 0
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)   # let the sampler start before the timed region
+    wall0 = time.perf_counter()
+    for ev in events:
+        step(ev)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in events]
+    prefix_ms = [e[0].elapsed_time(e[1]) for e in events]
+    tot_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    kv_bytes = w.kv_bytes()
+    value = kv_bytes * args.steps * world / (tot_ms * 1e-3) / 1e9
+    ms_per_step = tot_ms / args.steps
+
+    # roofline of the step and of the prefix kernel (dominant)
+    peaks, peak_kind = load_peaks()
+    hbm = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    flops = w.flops()
+    t_roof = max(w.algorithmic_bytes() / hbm, flops / tc)
+    prefix_s = statistics.mean(prefix_ms) * 1e-3
+    bound = "tensor" if flops / tc >= w.algorithmic_bytes() / hbm else "hbm"
+    if bound == "tensor":
+        achieved, peak, unit = flops / prefix_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = w.algorithmic_bytes() / prefix_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    traffic = recorded_traffic(name)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if rank >= 0:
+        host = {k: d[k].cpu().pin_memory() for k in ("q", "slot_idx", "prefix_len", "tree_parent", "tree_slot_idx")}
+        dbuf = {k: torch.empty_like(d[k]) for k in host}
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = h_out.numel() * 4 + h_lse.numel() * 4
+        e2e_ms = []
+        for i in range(args.warmup + max(10, args.steps // 10)):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k in host:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            v(dbuf["q"], d["kv_pool"], dbuf["slot_idx"], dbuf["prefix_len"], dbuf["tree_parent"],
+              dbuf["tree_slot_idx"], w.sm_scale, out=out, lse=lse)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+        e2e_s = statistics.mean(e2e_ms) * 1e-3
+        e2e = {"value": kv_bytes * world / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        s_per_row, rows_timed, threads = oracle_sample_rate(w, budget_s=args.cpu_budget)
+        step_s = s_per_row * w.batch * w.rows_per_request
+        cpu = {"value": kv_bytes / step_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows_timed} of {w.batch * w.rows_per_request} rows of one step, "
+                         f"time scaled by rows to a full step ({step_s:.1f} s)"}
+
+    if rank == 0:
+        us = sorted(x * 1e3 for x in step_ms)
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w, name, layout),
+            "us_per_step": {"mean": ms_per_step * 1e3, "median": statistics.median(us), "min": us[0]},
+            "roofline_step": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (ms_per_step * 1e-3),
+                              "bound": bound, "peaks": peak_kind},
+            "roofline": {"kernel": "prefix_attn_kernel", "bound": bound, "achieved": achieved, "peak": peak,
+                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                         "peak_kind": f"{peak_kind} (burst)"},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk, "wall_s": wall,
+            "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(wl.CONFIGS), default="c2")
+    ap.add_argument("--slots", choices=["perm", "churn", "contiguous"], default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-rows", type=int, default=64)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -120,6 +120,30 @@ DDT_API int ddtree_verify_attn(const void* q, const void* kv_pool, const int32_t
                        ddt_stream_t stream);
 
 /*
+ * The two phases of ddtree_verify_attn, for callers that schedule them
+ * separately (for example to overlap the second with other work, or to time
+ * each).  ddtree_verify_attn is exactly: clear the status word, then
+ * ddtree_verify_prefix_phase, then ddtree_verify_merge_phase, on one stream.
+ *   prefix phase: split-KV attention of every row over its prefix keys; writes
+ *                 one normalised partial (o, lse) per key split into the
+ *                 workspace.  Clears the status word first.
+ *   merge phase:  tree tail (ancestors and self) and the log-sum-exp merge of
+ *                 the tail with the prefix partials; writes out and lse.
+ * Both take the same arguments and checks as ddtree_verify_attn; the merge
+ * phase must follow the prefix phase of the same call on the same workspace.
+ */
+DDT_API int ddtree_verify_prefix_phase(const void* q, const void* kv_pool, const int32_t* slot_idx,
+                               const int32_t* prefix_len, const int32_t* tree_parent,
+                               const int32_t* tree_slot_idx, float sm_scale, float* out, float* lse,
+                               const ddt_dims* dims, void* workspace, size_t workspace_bytes,
+                               ddt_stream_t stream);
+DDT_API int ddtree_verify_merge_phase(const void* q, const void* kv_pool, const int32_t* slot_idx,
+                              const int32_t* prefix_len, const int32_t* tree_parent,
+                              const int32_t* tree_slot_idx, float sm_scale, float* out, float* lse,
+                              const ddt_dims* dims, void* workspace, size_t workspace_bytes,
+                              ddt_stream_t stream);
+
+/*
  * KV compaction (defragmentation) of each request's prefix rows
  * ("The Anatomy of a Kernel Investigation", section "The Reasoning Process: A
  * Deep Dive", phase 3; "The Architecture Detective", section "Defragmentation:

@@ -97,11 +97,15 @@ extern "C" size_t ddtree_verify_workspace_bytes(const ddt_dims* dims) {
   return plan.bytes;
 }
 
-extern "C" int ddtree_verify_attn(const void* q, const void* kv_pool, const int32_t* slot_idx,
-                                  const int32_t* prefix_len, const int32_t* tree_parent,
-                                  const int32_t* tree_slot_idx, float sm_scale, float* out, float* lse,
-                                  const ddt_dims* dims, void* workspace, size_t workspace_bytes,
-                                  ddt_stream_t stream) {
+namespace ddt {
+namespace {
+
+enum Phase : int { kPhasePrefix = 1, kPhaseMerge = 2 };
+
+int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t* slot_idx,
+                  const int32_t* prefix_len, const int32_t* tree_parent, const int32_t* tree_slot_idx,
+                  float sm_scale, float* out, float* lse, const ddt_dims* dims, void* workspace,
+                  size_t workspace_bytes, ddt_stream_t stream) {
   int rc = check_dims(dims);
   if (rc != DDT_OK) return rc;
   if (dims->batch == 0) return DDT_OK;
@@ -121,55 +125,73 @@ extern "C" int ddtree_verify_attn(const void* q, const void* kv_pool, const int3
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
-  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
-
   const float scale_log2 = sm_scale * 1.4426950408889634f;
   float* lse_part = reinterpret_cast<float*>(ws + plan.lse_off);
   float* o_part = reinterpret_cast<float*>(ws + plan.o_off);
 
-  if (plan.splits > 0) {
-    PrefixParams pp;
-    pp.q = static_cast<const uint16_t*>(q);
-    pp.kv = static_cast<const uint16_t*>(kv_pool);
-    pp.slot_idx = slot_idx;
-    pp.prefix_len = prefix_len;
-    pp.pool_slots = dims->pool_slots;
-    pp.slot_stride = dims->slot_stride;
-    pp.rows = plan.rows;
-    pp.row_tiles = plan.row_tiles;
-    pp.chunk = plan.chunk;
-    pp.max_splits = plan.splits;
-    pp.max_prefix_len = dims->max_prefix_len;
-    pp.scale_log2 = scale_log2;
-    pp.o_part = o_part;
-    pp.lse_part = lse_part;
-    pp.status = status;
-    if (launch_prefix(pp, dims->batch, plan.splits, s) != cudaSuccess) return DDT_ERR_LAUNCH;
+  if (phases & kPhasePrefix) {
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
+    if (plan.splits > 0) {
+      PrefixParams pp;
+      pp.q = static_cast<const uint16_t*>(q);
+      pp.kv = static_cast<const uint16_t*>(kv_pool);
+      pp.slot_idx = slot_idx;
+      pp.prefix_len = prefix_len;
+      pp.pool_slots = dims->pool_slots;
+      pp.slot_stride = dims->slot_stride;
+      pp.rows = plan.rows;
+      pp.row_tiles = plan.row_tiles;
+      pp.chunk = plan.chunk;
+      pp.max_splits = plan.splits;
+      pp.max_prefix_len = dims->max_prefix_len;
+      pp.scale_log2 = scale_log2;
+      pp.o_part = o_part;
+      pp.lse_part = lse_part;
+      pp.status = status;
+      if (launch_prefix(pp, dims->batch, plan.splits, s) != cudaSuccess) return DDT_ERR_LAUNCH;
+    }
   }
-
-  TailParams tp;
-  tp.q = static_cast<const uint16_t*>(q);
-  tp.kv = static_cast<const uint16_t*>(kv_pool);
-  tp.prefix_len = prefix_len;
-  tp.tree_parent = tree_parent;
-  tp.tree_slot_idx = tree_slot_idx;
-  tp.pool_slots = dims->pool_slots;
-  tp.nodes = dims->num_nodes;
-  tp.heads = dims->num_heads;
-  tp.heads_per_cta = dims->num_heads < 16 ? dims->num_heads : 16;
-  tp.row_tiles = plan.row_tiles;
-  tp.chunk = plan.chunk;
-  tp.max_splits = plan.splits;
-  tp.max_prefix_len = dims->max_prefix_len;
-  tp.scale_log2 = scale_log2;
-  tp.o_part = o_part;
-  tp.lse_part = lse_part;
-  tp.out = out;
-  tp.lse = lse;
-  tp.status = status;
-  if (launch_tail_merge(tp, dims->batch, s) != cudaSuccess) return DDT_ERR_LAUNCH;
+  if (phases & kPhaseMerge) {
+    TailParams tp;
+    tp.q = static_cast<const uint16_t*>(q);
+    tp.kv = static_cast<const uint16_t*>(kv_pool);
+    tp.prefix_len = prefix_len;
+    tp.tree_parent = tree_parent;
+    tp.tree_slot_idx = tree_slot_idx;
+    tp.pool_slots = dims->pool_slots;
+    tp.nodes = dims->num_nodes;
+    tp.heads = dims->num_heads;
+    tp.heads_per_cta = dims->num_heads < 16 ? dims->num_heads : 16;
+    tp.row_tiles = plan.row_tiles;
+    tp.chunk = plan.chunk;
+    tp.max_splits = plan.splits;
+    tp.max_prefix_len = dims->max_prefix_len;
+    tp.scale_log2 = scale_log2;
+    tp.o_part = o_part;
+    tp.lse_part = lse_part;
+    tp.out = out;
+    tp.lse = lse;
+    tp.status = status;
+    if (launch_tail_merge(tp, dims->batch, s) != cudaSuccess) return DDT_ERR_LAUNCH;
+  }
   return DDT_OK;
 }
+
+}  // namespace
+}  // namespace ddt
+
+#define DDT_VERIFY_ARGS                                                                                     \
+  const void *q, const void *kv_pool, const int32_t *slot_idx, const int32_t *prefix_len,                  \
+      const int32_t *tree_parent, const int32_t *tree_slot_idx, float sm_scale, float *out, float *lse,      \
+      const ddt_dims *dims, void *workspace, size_t workspace_bytes, ddt_stream_t stream
+#define DDT_VERIFY_PASS \
+  q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out, lse, dims, workspace, workspace_bytes, stream
+
+extern "C" int ddtree_verify_attn(DDT_VERIFY_ARGS) {
+  return verify_phases(kPhasePrefix | kPhaseMerge, DDT_VERIFY_PASS);
+}
+extern "C" int ddtree_verify_prefix_phase(DDT_VERIFY_ARGS) { return verify_phases(kPhasePrefix, DDT_VERIFY_PASS); }
+extern "C" int ddtree_verify_merge_phase(DDT_VERIFY_ARGS) { return verify_phases(kPhaseMerge, DDT_VERIFY_PASS); }
 
 extern "C" int ddtree_kv_compact(const void* kv_src, void* kv_dst, const int32_t* slot_idx,
                                  const int32_t* prefix_len, const int64_t* dst_start, int32_t* slot_idx_out,

@@ -23,8 +23,8 @@ STATUS_BAD_PARENT = 2
 STATUS_BAD_PREFIX = 4
 STATUS_TIMEOUT = 8
 
-EXPORTS = ("ddtree_verify_workspace_bytes", "ddtree_verify_attn", "ddtree_kv_compact",
-           "ddtree_read_device_status", "ddtree_status_string")
+EXPORTS = ("ddtree_verify_workspace_bytes", "ddtree_verify_attn", "ddtree_verify_prefix_phase",
+           "ddtree_verify_merge_phase", "ddtree_kv_compact", "ddtree_read_device_status", "ddtree_status_string")
 
 
 class DDTError(RuntimeError):
@@ -52,9 +52,11 @@ def lib():
         vp, i32p = ctypes.c_void_p, ctypes.c_void_p
         L.ddtree_verify_workspace_bytes.restype = ctypes.c_size_t
         L.ddtree_verify_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
-        L.ddtree_verify_attn.restype = ctypes.c_int
-        L.ddtree_verify_attn.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp,
-                                         ctypes.POINTER(Dims), vp, ctypes.c_size_t, vp]
+        for fn in ("ddtree_verify_attn", "ddtree_verify_prefix_phase", "ddtree_verify_merge_phase"):
+            f = getattr(L, fn)
+            f.restype = ctypes.c_int
+            f.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp, ctypes.POINTER(Dims), vp,
+                          ctypes.c_size_t, vp]
         L.ddtree_kv_compact.restype = ctypes.c_int
         L.ddtree_kv_compact.argtypes = [vp, vp, i32p, i32p, vp, i32p, ctypes.POINTER(Dims), vp, vp]
         L.ddtree_read_device_status.restype = ctypes.c_int
@@ -111,18 +113,21 @@ class Verifier:
             self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device)
 
     def __call__(self, q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out=None,
-                 lse=None, stream=None):
+                 lse=None, stream=None, phase="all"):
+        """phase: "all" (ddtree_verify_attn), "prefix" or "merge" (the two halves of it)."""
         import torch
         B, T, H, D = q.shape
         if out is None:
             out = torch.empty((B, T, H, D_V), dtype=torch.float32, device=q.device)
         if lse is None:
             lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
-        rc = lib().ddtree_verify_attn(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len), _ptr(tree_parent),
-                                      _ptr(tree_slot_idx), float(sm_scale), _ptr(out), _ptr(lse),
-                                      ctypes.byref(self.dims), _ptr(self.workspace), self.workspace.numel(),
-                                      _stream(stream))
-        _check(rc, "ddtree_verify_attn")
+        fn = {"all": "ddtree_verify_attn", "prefix": "ddtree_verify_prefix_phase",
+              "merge": "ddtree_verify_merge_phase"}[phase]
+        rc = getattr(lib(), fn)(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len), _ptr(tree_parent),
+                                _ptr(tree_slot_idx), float(sm_scale), _ptr(out), _ptr(lse),
+                                ctypes.byref(self.dims), _ptr(self.workspace), self.workspace.numel(),
+                                _stream(stream))
+        _check(rc, fn)
         return out, lse
 
     def status(self, stream=None) -> int:

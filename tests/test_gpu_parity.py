@@ -104,11 +104,12 @@ def test_edge_cases(prefix, nodes, heads, tree):
 
 
 def test_deterministic_and_layout_invariant():
-    w = wl.make_workload("tiny", prefix=(4099,), nodes=33, heads=16, max_depth=6, max_branch=4)
+    kw = dict(prefix=(4099,), nodes=33, heads=16, max_depth=6, max_branch=4, pool_slots=1 << 16)
+    w = wl.make_workload("tiny", **kw)
     o1, l1, _, d = run_gpu(w)
     o2, l2, _, _ = run_gpu(w, dev=d)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    wc = wl.make_workload("tiny", prefix=(4099,), nodes=33, heads=16, max_depth=6, max_branch=4, slots="contiguous")
+    wc = wl.make_workload("tiny", slots="contiguous", **kw)
     o3, l3, _, _ = run_gpu(wc)
     assert torch.equal(o1, o3) and torch.equal(l1, l3)
 
