@@ -36,7 +36,7 @@ from speculative_decoding_tree_05_gb300 import workloads as wl  # noqa: E402
 METRIC = "verify-attn µs/step and effective KV GB/s (fraction of GB300 roofline)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-PREFIX_SRC = os.path.join(ROOT, "speculative_decoding_tree_05_gb300", "csrc", "prefix_attn.cu")
+PREFIX_SRC = os.path.join(ROOT, "speculative_decoding_tree_05_gb300", "csrc", "prefix_pair.cu")
 
 
 def load_peaks():
@@ -56,7 +56,7 @@ def source_digest(path):
 def recorded_traffic(workload):
     """DRAM bytes per prefix-kernel launch from a committed ncu summary, if it was
     taken on the current kernel source; else None."""
-    path = os.path.join(PROFILE_DIR, f"prefix_attn_{workload}.txt")
+    path = os.path.join(PROFILE_DIR, f"prefix_pair_{workload}.txt")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -288,7 +288,7 @@ def run_ours(args, rank, world, local_rank):
             "us_per_step": {"mean": ms_per_step * 1e3, "median": statistics.median(us), "min": us[0]},
             "roofline_step": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (ms_per_step * 1e-3),
                               "bound": bound, "peaks": peak_kind},
-            "roofline": {"kernel": "prefix_attn_kernel", "bound": bound, "achieved": achieved, "peak": peak,
+            "roofline": {"kernel": "prefix_pair_kernel", "bound": bound, "achieved": achieved, "peak": peak,
                          "unit": unit, "frac": achieved / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} (burst)"},
             "gpu_launches": 2 * args.steps,

@@ -1,5 +1,6 @@
 // api.cu -- the extern "C" boundary: argument checks, workspace plan, launches.
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <mutex>
 #include "../../include/ddtree.h"
 #include "kernels.cuh"
@@ -63,14 +64,26 @@ int make_plan(const ddt_dims* d, int sm_count, Plan* plan) {
   p.row_tiles = (p.rows + kTileRows - 1) / kTileRows;
   const int64_t L = d->max_prefix_len;
   if (L > 0 && d->batch > 0) {
-    const int64_t ctas_per_split = int64_t(d->batch) * p.row_tiles * 2;
-    const int64_t target = 2 * int64_t(sm_count);
-    int64_t splits = (target + ctas_per_split - 1) / ctas_per_split;
-    const int64_t max_tiles = (L + kKeysPerTile - 1) / kKeysPerTile;
-    if (splits > max_tiles) splits = max_tiles;
-    if (splits < 1) splits = 1;
-    int64_t chunk = (L + splits - 1) / splits;
-    chunk = (chunk + kKeysPerTile - 1) / kKeysPerTile * kKeysPerTile;
+    // Pick the number of key splits that fills the GPU's CTA pairs in whole
+    // waves (each unit = one pair on one (request, row tile, split)); among
+    // equally good choices take the fewest splits.  Splits are at least
+    // kMinChunk keys long so per-unit set-up stays small.
+    const int64_t pairs = sm_count >= 2 ? sm_count / 2 : 1;
+    const int64_t per_split = int64_t(d->batch) * p.row_tiles;
+    const int64_t tiles = (L + kKeysPerTile - 1) / kKeysPerTile;
+    const int64_t max_splits = std::max<int64_t>(1, std::min<int64_t>(64, (L + kMinChunk - 1) / kMinChunk));
+    int64_t best = 1;
+    double best_eff = -1.0;
+    for (int64_t s = 1; s <= max_splits; ++s) {
+      const int64_t units = per_split * s;
+      const int64_t waves = (units + pairs - 1) / pairs;
+      const double eff = double(units) / double(waves * pairs);
+      if (eff > best_eff + 1e-9) {
+        best_eff = eff;
+        best = s;
+      }
+    }
+    int64_t chunk = (tiles + best - 1) / best * kKeysPerTile;
     p.chunk = static_cast<int>(chunk);
     p.splits = static_cast<int>((L + chunk - 1) / chunk);
   }

@@ -71,14 +71,10 @@ struct CompactParams {
   int32_t* status;
 };
 
-// Prefix kernel geometry.
-constexpr int kTileRows = 128;            // query rows per CTA (tcgen05 M)
-constexpr int kKeysPerTile = 32;          // keys per pipeline step (S tile N)
-constexpr int kPrefixThreads = 128;
-constexpr int kQBytes = kTileRows * kRowBytes;           // 147456
-constexpr int kKTileBytes = kKeysPerTile * kRowBytes;    // 36864
-constexpr int kPBytes = kTileRows * kKeysPerTile * 2;    // 8192
-constexpr int kPrefixSmem = kQBytes + 2 * kKTileBytes + kPBytes + 1024;
+// Prefix kernel geometry: a pair of CTAs per 128-row tile, 32 keys per step.
+constexpr int kTileRows = 128;            // query rows per CTA pair (tcgen05 M)
+constexpr int kKeysPerTile = 32;          // keys per pipeline step
+constexpr int kMinChunk = 256;            // shortest key split the planner makes
 
 // Per-device set-up (shared-memory opt-in), called once per device before launches.
 cudaError_t configure_prefix();

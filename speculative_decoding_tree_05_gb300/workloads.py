@@ -338,6 +338,9 @@ def to_device(w: Workload, device="cuda", poison: bool = True):
     """
     import torch
 
+    used = w.used_slots()
+    if len(used) and (used.min() < 0 or used.max() >= w.pool_slots):
+        raise ValueError("slot index outside the pool; corrupt slot tables after upload, not before")
     fill = BF16_NAN if poison else 0
     pool = torch.full((w.pool_slots, D_QK), fill, dtype=torch.int16, device=device)
     for b in range(w.batch):

@@ -118,9 +118,9 @@ def test_deterministic_and_layout_invariant():
 
 def test_bad_slot_is_masked_and_reported():
     w = wl.make_workload("tiny", prefix=(300,))
-    w.slot_idx[0, 77] = w.pool_slots + 12
-    w.tree_slot_idx[0, 3] = -5
     d = wl.to_device(w, "cuda")
+    d["slot_idx"][0, 77] = w.pool_slots + 12     # corrupted after upload: the kernels must mask them
+    d["tree_slot_idx"][0, 3] = -5
     out, lse, st, _ = run_gpu(w, dev=d)
     assert st & ddtree.STATUS_BAD_SLOT
     pool, si, ts = w.compact_host_pool()
