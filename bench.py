@@ -67,6 +67,22 @@ def recorded_traffic(workload):
     return float(m_b.group(1))
 
 
+def max_over_ranks(x, device=None):
+    """Largest value of x over all ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_gbs(kv_bytes_per_step, steps, world, max_ms):
+    """Whole-job effective KV GB/s: every rank's rows over the slowest rank's time."""
+    return kv_bytes_per_step * steps * world / (max_ms * 1e-3) / 1e9
+
+
 def workload_config(w, name, layout):
     return {"workload": f"{name}: {wl.DESCRIPTIONS[name]}", "batch": w.batch, "prefix_len_total": int(w.prefix_len.sum()),
             "tree_nodes": w.nodes, "heads": w.heads, "d_qk": wl.D_QK, "d_v": wl.D_V, "pool_slots": w.pool_slots,
@@ -219,13 +235,9 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[2]) for e in events]
     prefix_ms = [e[0].elapsed_time(e[1]) for e in events]
-    tot_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(step_ms), dev)
     kv_bytes = w.kv_bytes()
-    value = kv_bytes * args.steps * world / (tot_ms * 1e-3) / 1e9
+    value = job_throughput_gbs(kv_bytes, args.steps, world, tot_ms)
     ms_per_step = tot_ms / args.steps
 
     # roofline of the step and of the prefix kernel (dominant)

@@ -174,7 +174,7 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
     tp.pool_slots = dims->pool_slots;
     tp.nodes = dims->num_nodes;
     tp.heads = dims->num_heads;
-    tp.heads_per_cta = dims->num_heads < 16 ? dims->num_heads : 16;
+    tp.heads_per_cta = dims->num_heads < 8 ? dims->num_heads : 8;
     tp.row_tiles = plan.row_tiles;
     tp.chunk = plan.chunk;
     tp.max_splits = plan.splits;

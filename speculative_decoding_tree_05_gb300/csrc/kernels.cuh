@@ -16,7 +16,7 @@ constexpr int32_t kStatusBadParent = 2;
 constexpr int32_t kStatusBadPrefix = 4;
 constexpr int32_t kStatusTimeout = 8;
 
-// Split-KV prefix pass: one CTA per (request, 128-row tile, v-half, key split).
+// Split-KV prefix pass: one CTA pair per (request, 128-row tile, key split).
 struct PrefixParams {
   const uint16_t* q;         // bf16 [B, T, H, 576]
   const uint16_t* kv;        // bf16 [N, 576]

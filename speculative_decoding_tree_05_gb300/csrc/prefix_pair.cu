@@ -24,7 +24,12 @@
 // Per CTA (256 threads):
 //   warp 0      TMEM allocation; lane 0 issues every tcgen05.mma
 //   warps 1-3   producers: gather the CTA's 576-byte half of 32 slot rows per
-//               step with 16-byte cp.async into an 8-stage ring
+//               step with 16-byte cp.async (swizzled on the fly) into an
+//               8-stage ring; the step's 32 slot indices are fetched one step
+//               ahead and passed between lanes by shuffle; each producer thread
+//               signals the stage with cp.async.mbarrier.arrive.noinc, so no
+//               producer ever waits for its own copies; rows of keys past the
+//               split end or outside the pool are zero-filled
 //   warps 4-7   softmax: one query row per thread (= its TMEM lane); Q_r is
 //               staged into TMEM first; online softmax in the log2 domain with
 //               lazy rescaling (O is rescaled only when the running max grows
@@ -46,12 +51,12 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kNk = 32;                                  // keys per step
 constexpr int kStages = 8;
-constexpr int kLag = 4;                                  // cp.async groups in flight per producer thread
-constexpr int kProducers = 96;
 constexpr int kLatBlock = kNk * 128;                     // 4096
 constexpr int kStageBytes = 4 * kLatBlock + kNk * 64;    // 18432
+constexpr int kProducers = 96;
 constexpr int kXBytes = kTileRows * kNk * 4;             // 16384: one fp32 partial-score tile
-constexpr int kSmem = kStages * kStageBytes + 2 * kXBytes + 1024;
+constexpr int kXBufs = 4;                                // exchange buffers (tile t uses t % 4)
+constexpr int kSmem = kStages * kStageBytes + kXBufs * kXBytes + 1024;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 352, kTmemCols = 512;
 constexpr uint32_t kIdescS = idesc_bf16_f32(kTileRows, kNk, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileRows, 256, false, true);
@@ -63,14 +68,15 @@ struct Shared {
   uint64_t k_empty[kStages];  // MMA -> producers: stage consumed (after P.V)
   uint64_t s_full[3];         // MMA -> softmax: partial scores in TMEM
   uint64_t p_ready[3];        // softmax -> MMA: P in TMEM, O rescaled
-  uint64_t x_full[2];         // peer -> softmax: peer's partial scores arrived
+  uint64_t x_full[kXBufs];    // peer -> softmax: peer's partial scores of tile t arrived (buffer t % 4)
   uint64_t pv_done[3];        // MMA -> softmax: P.V of step i completes phase i/3 of pv_done[i%3]
   uint64_t q_ready;           // softmax -> MMA: Q_r staged in TMEM
   uint32_t tmem_base;
   int abort;
 };
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_pair_kernel(PrefixParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    prefix_pair_kernel(const __grid_constant__ PrefixParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   volatile int* abort = &sh.abort;
@@ -104,8 +110,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.p_ready[i], 128);
     }
-    mbar_init(&sh.x_full[0], 1);
-    mbar_init(&sh.x_full[1], 1);
+    for (int i = 0; i < kXBufs; ++i) mbar_init(&sh.x_full[i], 1);
     for (int i = 0; i < 3; ++i) mbar_init(&sh.pv_done[i], 1);
     mbar_init(&sh.q_ready, 128);
     sh.abort = 0;
@@ -130,6 +135,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         if (j < ntiles) {
           const int st = j % kStages;
           if (!mbar_wait_abortable(&sh.k_full[st], (j / kStages) & 1, abort)) { ok = false; break; }
+          // the stage was written by cp.async (generic proxy): order it before the
+          // tensor core's async-proxy reads
+          fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t base = stage0 + st * kStageBytes;
           const uint32_t sb = tmem + kColS + (j % 3) * kNk;
@@ -167,45 +175,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     const int ptid = tid - 32;
     const int32_t* slots = p.slot_idx + static_cast<int64_t>(b) * p.slot_stride;
     const uint16_t* kv = p.kv;
-    int j = 0;
-    for (; j < ntiles; ++j) {
+    // lane l holds the slot of key l of a step (fetched one step ahead)
+    auto fetch = [&](int j) -> int {
+      const int key = kbegin + j * kNk + lane;
+      return key < kend ? __ldg(slots + key) : -1;
+    };
+    int slot_cur = fetch(0);
+    for (int j = 0; j < ntiles; ++j) {
+      const int slot_next = (j + 1 < ntiles) ? fetch(j + 1) : -1;
       const int st = j % kStages;
-      if (j >= kStages && !mbar_wait_abortable(&sh.k_empty[st], ((j / kStages) - 1) & 1, abort)) {
+      // warp-uniform wait: the lane shuffles below need every lane
+      const bool waited = j < kStages || mbar_wait_abortable(&sh.k_empty[st], ((j / kStages) - 1) & 1, abort);
+      if (!__all_sync(0xffffffffu, waited)) {
         ok = false;
         break;
       }
       const int kbase = kbegin + j * kNk;
+      if (warp == 1 && rank == 0) {
+        const bool bad = kbase + lane < kend && (slot_cur < 0 || static_cast<int64_t>(slot_cur) >= p.pool_slots);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kStatusBadSlot);
+      }
       const uint32_t base = stage0 + st * kStageBytes;
-#pragma unroll 4
-      for (int i = ptid; i < kNk * 36; i += kProducers) {
+#pragma unroll
+      for (int k = 0; k < kNk * 36 / kProducers; ++k) {
+        const int i = ptid + k * kProducers;
         const int n = i / 36, c = i - n * 36;
-        const int key = kbase + n;
-        const uint16_t* src = kv;
-        uint32_t bytes = 0;
-        if (key < kend) {
-          const int32_t slot = __ldg(slots + key);
-          if (slot >= 0 && static_cast<int64_t>(slot) < p.pool_slots) {
-            const int off = (c < 32) ? 256 * static_cast<int>(rank) + 8 * c : 512 + 32 * static_cast<int>(rank) + 8 * (c - 32);
-            src = kv + static_cast<int64_t>(slot) * kDqk + off;
-            bytes = 16;
-          } else if (c == 0 && rank == 0) {
-            atomicOr(p.status, kStatusBadSlot);
-          }
-        }
+        const int slot = __shfl_sync(0xffffffffu, slot_cur, n);
+        const bool valid = slot >= 0 && static_cast<int64_t>(slot) < p.pool_slots;
+        const int off = (c < 32) ? 256 * static_cast<int>(rank) + 8 * c : 512 + 32 * static_cast<int>(rank) + 8 * (c - 32);
+        const uint16_t* src = valid ? kv + static_cast<int64_t>(slot) * kDqk + off : kv;
         const uint32_t dst = (c < 32) ? base + (c >> 3) * kLatBlock + n * 128 + (((c & 7) ^ (n & 7)) << 4)
                                       : base + 4 * kLatBlock + n * 64 + (((c - 32) ^ ((n >> 1) & 3)) << 4);
-        cp_async16(dst, src, bytes);
+        cp_async16(dst, src, valid ? 16u : 0u);
       }
-      cp_async_commit();
-      if (j >= kLag) {
-        cp_async_wait<kLag>();
-        fence_proxy_async_smem();
-        mbar_arrive(&sh.k_full[(j - kLag) % kStages]);
-      }
+      cp_async_arrive_noinc(&sh.k_full[st]);
+      slot_cur = slot_next;
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (int t = (j > kLag ? j - kLag : 0); t < j; ++t) mbar_arrive(&sh.k_full[t % kStages]);
   } else {
     // ------------------------------------------------------------------ softmax + epilogue
     const int r = tid - 128;
@@ -239,44 +245,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     }
 
     const uint32_t peer = rank ^ 1u;
-    const uint32_t x_remote[2] = {mapa_shared(smem_u32(xbuf), peer), mapa_shared(smem_u32(xbuf + kXBytes), peer)};
-    const uint32_t xbar_remote[2] = {mapa_shared(smem_u32(&sh.x_full[0]), peer),
-                                     mapa_shared(smem_u32(&sh.x_full[1]), peer)};
+    uint32_t x_remote[kXBufs], xbar_remote[kXBufs];
+#pragma unroll
+    for (int i = 0; i < kXBufs; ++i) {
+      x_remote[i] = mapa_shared(smem_u32(xbuf + i * kXBytes), peer);
+      xbar_remote[i] = mapa_shared(smem_u32(&sh.x_full[i]), peer);
+    }
     const int32_t* slots = p.slot_idx + static_cast<int64_t>(b) * p.slot_stride;
     const uint32_t rsw = static_cast<uint32_t>(r & 7);
     float m_used = -CUDART_INF_F, l = 0.f;
+    auto fetch_slot = [&](int j) -> int {
+      const int key = kbegin + j * kNk + lane;
+      return key < kend ? __ldg(slots + key) : 0;
+    };
+    int slot_pf[2] = {fetch_slot(0), fetch_slot(1)};
+
+    // Score exchange, software-pipelined by one step: the partial scores of
+    // step j+1 are loaded from TMEM and sent to the peer before step j is
+    // finished, so the DSMEM transfer overlaps the softmax of step j.  Step t
+    // uses exchange buffer t % 4; the peer writes step t only after it has
+    // received our step t-2, which we send after finishing step t-4, the last
+    // reader of that buffer.
+    float own[32], own_next[32];
+    auto load_and_send = [&](int t, float (&dst)[32]) -> bool {
+      if (r == 0) mbar_arrive_expect_tx(&sh.x_full[t % kXBufs], kXBytes);
+      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.s_full[t % 3], (t / 3) & 1, abort))) return false;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + kColS + (t % 3) * kNk, dst);
+      const uint32_t xr = x_remote[t % kXBufs] + r * 128, br = xbar_remote[t % kXBufs];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = make_uint4(__float_as_uint(dst[4 * c]), __float_as_uint(dst[4 * c + 1]),
+                                   __float_as_uint(dst[4 * c + 2]), __float_as_uint(dst[4 * c + 3]));
+        st_async_v4(xr + ((c ^ rsw) << 4), v, br);
+      }
+      return true;
+    };
+    if (!load_and_send(0, own)) ok = false;
 
     for (int j = 0; ok && j < ntiles; ++j) {
       const int sb = j % 3;
       const int kbase = kbegin + j * kNk;
-      uint32_t masked;
-      {
-        const int key = kbase + lane;
-        bool bad = key >= kend;
-        if (!bad) {
-          const int32_t slot = __ldg(slots + key);
-          bad = slot < 0 || static_cast<int64_t>(slot) >= p.pool_slots;
-        }
-        masked = __ballot_sync(0xffffffffu, bad);
-      }
-      if (r == 0) mbar_arrive_expect_tx(&sh.x_full[j & 1], kXBytes);
-      // waits are made warp-uniform: tcgen05.ld/st below need the whole warp
-      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.s_full[sb], (j / 3) & 1, abort))) { ok = false; break; }
-      tc_fence_after();
-      float s[32];
-      tmem_ld32(tmem + lane_off + kColS + sb * kNk, s);
-      // my partial row -> the peer's exchange buffer (row r, 16-byte chunks XOR-swizzled by r & 7)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = make_uint4(__float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
-                                   __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]));
-        st_async_v4(x_remote[j & 1] + r * 128 + ((c ^ rsw) << 4), v, xbar_remote[j & 1]);
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_full[j & 1], (j >> 1) & 1, abort, true))) {
+      if (j + 1 < ntiles && !load_and_send(j + 1, own_next)) { ok = false; break; }
+      // key mask of this step (past the split end or a slot outside the pool); the
+      // slot of this lane's key was fetched two steps ago
+      const int slot_j = slot_pf[0];
+      slot_pf[0] = slot_pf[1];
+      slot_pf[1] = fetch_slot(j + 2);
+      const uint32_t masked = __ballot_sync(
+          0xffffffffu, kbase + lane >= kend || slot_j < 0 || static_cast<int64_t>(slot_j) >= p.pool_slots);
+      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_full[j % kXBufs], (j / kXBufs) & 1, abort, true))) {
         ok = false;
         break;
       }
-      const uint8_t* xb = xbuf + (j & 1) * kXBytes + r * 128;
+      const uint8_t* xb = xbuf + (j % kXBufs) * kXBytes + r * 128;
+      float sc[32];
       float mx = -CUDART_INF_F;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -285,9 +308,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int k = 4 * c + e;
-          const float x = (s[k] + pv[e]) * p.scale_log2;
-          s[k] = ((masked >> k) & 1u) ? -CUDART_INF_F : x;
-          mx = fmaxf(mx, s[k]);
+          const float x = (own[k] + pv[e]) * p.scale_log2;
+          sc[k] = ((masked >> k) & 1u) ? -CUDART_INF_F : x;
+          mx = fmaxf(mx, sc[k]);
         }
       }
       const bool need = mx > m_used + kRescaleThreshold;
@@ -319,7 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       uint32_t pk[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const float p0 = fast_exp2(s[2 * e] - msub), p1 = fast_exp2(s[2 * e + 1] - msub);
+        const float p0 = fast_exp2(sc[2 * e] - msub), p1 = fast_exp2(sc[2 * e + 1] - msub);
         sum += p0 + p1;
         pk[e] = pack_bf16x2(p0, p1);
       }
@@ -327,6 +350,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       tmem_st16(tmem + lane_off + kColS + sb * kNk, pk);
       tc_fence_before();
       mbar_arrive(&sh.p_ready[sb]);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) own[k] = own_next[k];
     }
 
     // epilogue: wait for the last P.V, then o = O / l and lse = (m + log2 l) ln 2
