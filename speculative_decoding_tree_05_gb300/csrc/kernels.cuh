@@ -73,7 +73,7 @@ struct CompactParams {
 
 // Prefix kernel geometry: a pair of CTAs per 128-row tile, 32 keys per step.
 constexpr int kTileRows = 128;            // query rows per CTA pair (tcgen05 M)
-constexpr int kKeysPerTile = 32;          // keys per pipeline step
+constexpr int kKeysPerTile = 64;          // keys per pipeline step
 constexpr int kMinChunk = 256;            // shortest key split the planner makes
 
 // Per-device set-up (shared-memory opt-in), called once per device before launches.

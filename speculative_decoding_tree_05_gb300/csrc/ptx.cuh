@@ -89,6 +89,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint4 v, uint3
                : "memory");
 }
 
+// 4-byte variant of st_async_v4.
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr), "r"(v),
+               "r"(remote_bar)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async (16 B, zero fill)
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
