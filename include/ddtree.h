@@ -162,6 +162,28 @@ DDT_API int ddtree_kv_compact(const void* kv_src, void* kv_dst, const int32_t* s
                       const int32_t* prefix_len, const int64_t* dst_start, int32_t* slot_idx_out,
                       const ddt_dims* dims, void* workspace, ddt_stream_t stream);
 
+/*
+ * Verify attention without any allocation, for callers that cannot allocate
+ * device memory when they run it (for example code running inside a memory
+ * pool or allocator callback, or a plugin that may only use the buffers its
+ * host framework hands it).  The pages have no counterpart of this entry point.
+ *
+ * Same arguments and results as ddtree_verify_attn, minus the workspace: the
+ * scratch lives in a fixed 32 MiB device array inside the library, which every
+ * GPU that loads the library holds until the process exits.  Sizes whose
+ * scratch (ddtree_verify_workspace_bytes) exceeds 32 MiB return
+ * DDT_ERR_WORKSPACE before anything is enqueued.  The first call on each device
+ * looks up the array's device address (once, with that device current); make
+ * that first call before any stream capture.  Every call shares the one array:
+ * calls whose work overlaps on the GPU (on different streams, or from several
+ * threads) race and must be serialised by the caller.  The device status word
+ * of these calls is not readable by the caller.
+ */
+DDT_API int ddtree_verify_attn_static_scratch(const void* q, const void* kv_pool, const int32_t* slot_idx,
+                                              const int32_t* prefix_len, const int32_t* tree_parent,
+                                              const int32_t* tree_slot_idx, float sm_scale, float* out,
+                                              float* lse, const ddt_dims* dims, ddt_stream_t stream);
+
 /* Waits for `stream`, then copies the status word of the last call that used
  * `workspace` to *host_status.  Returns DDT_OK or DDT_ERR_*. */
 DDT_API int ddtree_read_device_status(const void* workspace, int32_t* host_status, ddt_stream_t stream);

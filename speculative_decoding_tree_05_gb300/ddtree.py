@@ -24,7 +24,8 @@ STATUS_BAD_PREFIX = 4
 STATUS_TIMEOUT = 8
 
 EXPORTS = ("ddtree_verify_workspace_bytes", "ddtree_verify_attn", "ddtree_verify_prefix_phase",
-           "ddtree_verify_merge_phase", "ddtree_kv_compact", "ddtree_read_device_status", "ddtree_status_string")
+           "ddtree_verify_merge_phase", "ddtree_verify_attn_static_scratch", "ddtree_kv_compact",
+           "ddtree_read_device_status", "ddtree_status_string")
 
 
 class DDTError(RuntimeError):
@@ -57,6 +58,9 @@ def lib():
             f.restype = ctypes.c_int
             f.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp, ctypes.POINTER(Dims), vp,
                           ctypes.c_size_t, vp]
+        L.ddtree_verify_attn_static_scratch.restype = ctypes.c_int
+        L.ddtree_verify_attn_static_scratch.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp,
+                                                        ctypes.POINTER(Dims), vp]
         L.ddtree_kv_compact.restype = ctypes.c_int
         L.ddtree_kv_compact.argtypes = [vp, vp, i32p, i32p, vp, i32p, ctypes.POINTER(Dims), vp, vp]
         L.ddtree_read_device_status.restype = ctypes.c_int
@@ -140,6 +144,23 @@ def verify_attn(q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm
     B, T, H, _ = q.shape
     v = Verifier(B, T, H, kv_pool.shape[0], slot_idx.shape[1], max_prefix_len, device=q.device)
     return v(q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out, lse, stream)
+
+
+def verify_attn_static_scratch(q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out,
+                               lse, max_prefix_len=None, stream=None):
+    """Verify attention with the library's fixed scratch array (no allocation in the call).
+
+    For callers that cannot allocate device memory at call time; out and lse
+    are caller-provided.  Calls must not overlap on the GPU (they share the array).
+    """
+    B, T, H, _ = q.shape
+    stride = slot_idx.shape[1]
+    dims = make_dims(B, T, H, kv_pool.shape[0], stride, stride if max_prefix_len is None else max_prefix_len)
+    rc = lib().ddtree_verify_attn_static_scratch(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len),
+                                                 _ptr(tree_parent), _ptr(tree_slot_idx), float(sm_scale), _ptr(out),
+                                                 _ptr(lse), ctypes.byref(dims), _stream(stream))
+    _check(rc, "ddtree_verify_attn_static_scratch")
+    return out, lse
 
 
 def kv_compact(kv_src, kv_dst, slot_idx, prefix_len, dst_start, slot_idx_out=None, max_prefix_len=None,
