@@ -1,4 +1,5 @@
 // api.cu -- the extern "C" boundary: argument checks, workspace plan, launches.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <mutex>
@@ -97,6 +98,37 @@ int make_plan(const ddt_dims* d, int sm_count, Plan* plan) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// cuTensorMapEncodeTiled, fetched from the driver once (no link-time libcuda dependency).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// The pool as a 2-D bf16 tensor [rows][576] (1152-byte rows), 128-byte swizzle,
+// box of 64 columns x box_rows rows.
+bool encode_pool_map(CUtensorMap* m, const void* pool, int64_t rows, uint32_t box_rows) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, elem_strides,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 }  // namespace ddt
 
@@ -146,6 +178,11 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
     if (plan.splits > 0) {
       PrefixParams pp;
+      // the 64-row block map (contiguous steps) only when the pool has 64 rows
+      pp.block_loads = dims->pool_slots >= kKeysPerTile ? 1 : 0;
+      if (!encode_pool_map(&pp.tmap_rows, kv_pool, dims->pool_slots, 1) ||
+          (pp.block_loads && !encode_pool_map(&pp.tmap_block, kv_pool, dims->pool_slots, kKeysPerTile)))
+        return DDT_ERR_LAUNCH;
       pp.q = static_cast<const uint16_t*>(q);
       pp.kv = static_cast<const uint16_t*>(kv_pool);
       pp.slot_idx = slot_idx;

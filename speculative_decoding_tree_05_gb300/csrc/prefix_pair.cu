@@ -25,28 +25,40 @@
 // round(x * 2^(14-e)), x being the partial score in log2 units.  That is half
 // the bytes of fp32 (the exchange is bound by DSMEM bandwidth) with an error of
 // at most 2^-15 * 2^e, i.e. 2^-14 of the row's largest partial in the step.
-// Both CTAs decode both halves the same way and add them in the same order, so
-// they hold bit-identical scores and make identical softmax decisions.
+// Rounding to an integer and packing use the float adder: x * 2^(14-e) + M with
+// M = 1.5 * 2^23 + 2^15 is an integer-valued float whose low 16 bits are the
+// biased mantissa, so no int/float conversion instruction is needed.  Both CTAs
+// decode both halves the same way and add them in the same order, so they hold
+// bit-identical scores and make identical softmax decisions.
 //
-// Per CTA (256 threads):
+// Per CTA (384 threads):
 //   warp 0      TMEM allocation; lane 0 issues every tcgen05.mma.  A
 //               tcgen05.mma costs about 45 issue cycles whatever its shape, so
 //               each MMA is at least M=128 x N=64 (scores) or N=256 (P.V).
-//   warps 1-3   producers: gather the CTA's 576-byte half of 64 slot rows per
-//               step with 16-byte cp.async (swizzled on the fly) into a 4-stage
-//               ring; slot indices are fetched one step ahead and passed
-//               between lanes by shuffle; each producer thread signals the
-//               stage with cp.async.mbarrier.arrive.noinc; rows of keys past
-//               the split end or outside the pool are zero-filled
-//   warps 4-7   softmax: one query row per thread (= its TMEM lane).  Q_r's
-//               256 latent dims are staged in TMEM and its 32 rope dims in
-//               shared memory; online softmax in the log2 domain with lazy
-//               rescaling (O is rescaled only when the running max grows by
-//               more than 8); P (bf16) is written over its S buffer and read
-//               from TMEM by the P.V MMA; epilogue o = O / l.
+//   warps 1-3   producers: load the CTA's dims of 64 slot rows per step into a
+//               3-stage ring, the step's slot indices fetched one step ahead.
+//               A step whose 64 slots are consecutive (a compacted pool) is 5
+//               tiled TMA boxes of 64 rows.  A scattered step uses TMA
+//               tile::gather4 for latent blocks 0-2 (16 lanes of each producer
+//               warp, one block per warp) and, at the same time, 16-byte
+//               cp.async from all 96 threads for latent block 3 and the rope
+//               dims: one SM's TMA unit and load/store path each gather
+//               scattered 128-byte row pieces at only ~14-19 B/clk, so both
+//               run at once.  A step with a key past the split end or a slot
+//               outside the pool is all cp.async with zero fill (its rows are
+//               masked and must not carry non-finite values into P.V).
+//   warps 4-7   softmax set 0 (even steps), warps 8-11 softmax set 1 (odd
+//               steps): one query row per thread (= its TMEM lane), so two
+//               steps are in flight at once.  The sets hand each other the
+//               running max of every row (step t waits for step t-1's); each
+//               set keeps its own row sums against the max it last used and
+//               the two are combined at the end.  O is rescaled in TMEM only
+//               when the running max grows by more than 8 (lazily); P (bf16)
+//               is written over its S buffer and read from TMEM by P.V.
 // TMEM columns: O_r [0,256), S buffers 2 x 64 at [256,384), Q_r latent [384,512).
-// Shared memory per stage: 4 latent blocks [64 keys][64 dims] (128-byte
-// swizzle, 8 KB each) + 1 rope block [64 keys][32 dims] (64-byte swizzle).
+// Shared memory per stage: 4 latent blocks [64 keys][64 dims] + 1 rope block
+// [64 keys][64 rope dims] (128-byte swizzle, 8 KB each; CTA r reads rope dims
+// [32r, 32r+32) of it).
 // The latent blocks are the K operand of S (K-major) and, read MN-major, the
 // V operand of P.V.
 #include <cuda_runtime.h>
@@ -57,32 +69,41 @@
 namespace ddt {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kNk = kKeysPerTile;                        // 64 keys per step
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kLatBlock = kNk * 128;                     // 8192
-constexpr int kRopeBlock = kNk * 64;                     // 4096
-constexpr int kStageBytes = 4 * kLatBlock + kRopeBlock;  // 36864
+constexpr int kStageBytes = 5 * kLatBlock;               // 40960: 4 latent blocks + the rope block
 constexpr int kProducers = 96;
+constexpr int kGatherBlocks = 3;                         // latent blocks fetched by gather4 on scattered steps
+constexpr int kXBufs = 4;                                // exchange buffers (step t uses t % 4)
 constexpr int kXBytes = kTileRows * kNk * 2;             // 16384: int16 mantissas of one step
 constexpr int kEBytes = kTileRows * 4;                   // 512: one exponent per row
 constexpr int kQRopeBytes = kTileRows * 64;              // 8192: Q_r rope dims, 64-byte swizzle
-constexpr int kSmemStages = kStages * kStageBytes;
-constexpr int kSmem = kSmemStages + 2 * kXBytes + 2 * kEBytes + kQRopeBytes + 1024;
+constexpr int kOffX = kStages * kStageBytes;
+constexpr int kOffE = kOffX + kXBufs * kXBytes;
+constexpr int kOffQRope = kOffE + kXBufs * kEBytes;
+constexpr int kOffHand = kOffQRope + kQRopeBytes;        // [2][128] running max handed between sets
+constexpr int kOffFin = kOffHand + 2 * kTileRows * 4;    // [2 sets][2 (l, m)][128] final row state
+constexpr int kSmem = kOffFin + 2 * 2 * kTileRows * 4 + 1024;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384, kTmemCols = 512;
 constexpr uint32_t kIdescS = idesc_bf16_f32(kTileRows, kNk, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileRows, 256, false, true);
 constexpr float kRescaleThreshold = 8.f;                 // log2 units
 constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kMagic = 12615680.0f;                    // 1.5 * 2^23 + 2^15
+constexpr uint32_t kMagicHi = 0x4B400000u;               // bits of 1.5 * 2^23
+constexpr int kSoftmaxBarrier = 1;                       // named barrier of the 256 softmax threads
 static_assert(kNk == 64, "the step layout assumes 64 keys");
 
 struct Shared {
   uint64_t k_full[kStages];   // producers -> MMA: stage loaded
   uint64_t k_empty[kStages];  // MMA -> producers: stage consumed (after P.V)
-  uint64_t s_full[2];         // MMA -> softmax: partial scores of step t in S buffer t % 2
-  uint64_t p_ready[2];        // softmax -> MMA: P of step t in S buffer t % 2, O rescaled
-  uint64_t x_full[2];         // peer -> softmax: peer's partial scores of step t in buffer t % 2
+  uint64_t s_full[2];         // MMA -> softmax set t%2: partial scores of step t in S buffer t % 2
+  uint64_t p_ready[2];        // softmax set -> MMA: P of step t in S buffer t % 2, O rescaled
+  uint64_t x_full[kXBufs];    // peer -> softmax: peer's partial scores of step t in buffer t % 4
   uint64_t pv_done[2];        // MMA -> softmax: P.V of step t completes phase t/2 of pv_done[t%2]
+  uint64_t m_ready[2];        // softmax set -> other set: running max after step t in hand[t % 2]
   uint64_t q_ready;           // softmax -> MMA: Q_r staged
   uint32_t tmem_base;
   int abort;
@@ -96,7 +117,7 @@ __device__ __forceinline__ int block_exponent(float amax) {
 }
 __device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(127 + k) << 23); }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_pair_kernel(PrefixParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_pair_kernel(const __grid_constant__ PrefixParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   volatile int* abort = &sh.abort;
@@ -119,23 +140,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t stage0 = smem_u32(smem);
-  uint8_t* xbuf = smem + kSmemStages;                          // [2][128 rows][128 B]
-  uint8_t* ebuf = xbuf + 2 * kXBytes;                          // [2][128 rows] int32
-  uint8_t* qrope = ebuf + 2 * kEBytes;                         // [128 rows][64 B], 64-byte swizzle
+  uint8_t* qrope = smem + kOffQRope;
   const uint32_t qrope_s = smem_u32(qrope);
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sh.k_full[i], kProducers);
+      mbar_init(&sh.k_full[i], kProducers + 1);  // every producer thread + one (TMA) arrival
       mbar_init(&sh.k_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.p_ready[i], 128);
-      mbar_init(&sh.x_full[i], 1);
       mbar_init(&sh.pv_done[i], 1);
+      mbar_init(&sh.m_ready[i], 128);
     }
-    mbar_init(&sh.q_ready, 128);
+    for (int i = 0; i < kXBufs; ++i) mbar_init(&sh.x_full[i], 1);
+    mbar_init(&sh.q_ready, 256);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -148,6 +168,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
   bool ok = true;
+  int issued = 0;  // producers: steps this warp has issued loads for
 
   if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer
@@ -174,7 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
           const uint64_t ad = smem_desc(qrope_s + ks * 32, 16, 512, kSwizzle64B);
-          const uint64_t bd = smem_desc(base + 4 * kLatBlock + ks * 32, 16, 512, kSwizzle64B);
+          const uint64_t bd = smem_desc(base + 4 * kLatBlock + 64 * rank + ks * 32, 16, 1024, kSwizzle128B);
           mma_ss(sb, ad, bd, kIdescS, 1u);
         }
         mma_commit(&sh.s_full[t % 2]);
@@ -202,11 +223,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     const int ptid = tid - 32;
     const int32_t* slots = p.slot_idx + static_cast<int64_t>(b) * p.slot_stride;
     const uint16_t* kv = p.kv;
-    // lane l holds the slots of keys l and l+32 of a step (fetched one step ahead)
+    const int rk = static_cast<int>(rank);
+    // lane l holds the slots of keys l and l+32 of a step (fetched one step ahead); -1 past the split end
     auto fetch = [&](int j, int e) -> int {
       const int key = kbegin + j * kNk + lane + 32 * e;
       return key < kend ? __ldg(slots + key) : -1;
     };
+    auto in_pool = [&](int s_) { return s_ >= 0 && static_cast<int64_t>(s_) < p.pool_slots; };
+    // 16-byte chunk c of the CTA's 48 per row -> (source column, smem offset in the stage):
+    // c < 32 latent block c/8, c >= 32 the CTA's rope chunks in the rope block
+    auto chunk_dst = [&](int n, int c) -> uint32_t {
+      return c < 32 ? (c >> 3) * kLatBlock + n * 128 + (((c & 7) ^ (n & 7)) << 4)
+                    : 4 * kLatBlock + n * 128 + (((4 * rk + c - 32) ^ (n & 7)) << 4);
+    };
+    auto chunk_col = [&](int c) -> int { return c < 32 ? 256 * rk + 8 * c : 512 + 32 * rk + 8 * (c - 32); };
     int cur0 = fetch(0, 0), cur1 = fetch(0, 1);
     for (int j = 0; j < ntiles; ++j) {
       const int nxt0 = (j + 1 < ntiles) ? fetch(j + 1, 0) : -1;
@@ -219,56 +249,98 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         break;
       }
       const int kbase = kbegin + j * kNk;
+      const bool v0 = kbase + lane < kend && in_pool(cur0), v1 = kbase + lane + 32 < kend && in_pool(cur1);
       if (warp == 1 && rank == 0) {
-        const bool bad0 = kbase + lane < kend && (cur0 < 0 || static_cast<int64_t>(cur0) >= p.pool_slots);
-        const bool bad1 = kbase + lane + 32 < kend && (cur1 < 0 || static_cast<int64_t>(cur1) >= p.pool_slots);
+        const bool bad0 = kbase + lane < kend && !in_pool(cur0), bad1 = kbase + lane + 32 < kend && !in_pool(cur1);
         if (__any_sync(0xffffffffu, bad0 || bad1) && lane == 0) atomicOr(p.status, kStatusBadSlot);
       }
+      const bool all_valid = __all_sync(0xffffffffu, v0 && v1);
+      const int first = __shfl_sync(0xffffffffu, cur0, 0);
+      const bool contiguous =
+          p.block_loads && all_valid && __all_sync(0xffffffffu, cur0 == first + lane && cur1 == first + 32 + lane);
       const uint32_t base = stage0 + st * kStageBytes;
+      if (contiguous) {
+        // 64 consecutive rows: five 64-row boxes (all latent blocks and the rope block)
+        if (warp == 1 && lane == 0) {
+          mbar_arrive_expect_tx(&sh.k_full[st], kStageBytes);
+#pragma unroll
+          for (int c = 0; c < 5; ++c)
+            tma_load_2d(base + c * kLatBlock, &p.tmap_block, c < 4 ? 256 * rk + 64 * c : 512, first, &sh.k_full[st]);
+        }
+      } else if (all_valid) {
+        // gather4 for latent blocks 0..2 (producer warp w takes block w-1) ...
+        if (warp == 1 && lane == 0) mbar_arrive_expect_tx(&sh.k_full[st], kGatherBlocks * kLatBlock);
+        int r[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int n = 4 * (lane & 15) + e;
+          const int s0 = __shfl_sync(0xffffffffu, cur0, n & 31), s1 = __shfl_sync(0xffffffffu, cur1, n & 31);
+          r[e] = n < 32 ? s0 : s1;
+        }
+        if (lane < 16) {
+          const int blk = warp - 1;
+          tma_gather4(base + blk * kLatBlock + lane * 512, &p.tmap_rows, 256 * rk + 64 * blk, r[0], r[1], r[2], r[3],
+                      &sh.k_full[st]);
+        }
+        // ... and cp.async for latent block 3 (chunks 24..31) and the rope chunks (32..35)
 #pragma unroll 4
-      for (int k = 0; k < kNk * 36 / kProducers; ++k) {
-        const int i = ptid + k * kProducers;
-        const int n = i / 36, c = i - n * 36;
-        const int s0 = __shfl_sync(0xffffffffu, cur0, n & 31);
-        const int s1 = __shfl_sync(0xffffffffu, cur1, n & 31);
-        const int slot = n < 32 ? s0 : s1;
-        const bool valid = slot >= 0 && static_cast<int64_t>(slot) < p.pool_slots;
-        const int off = (c < 32) ? 256 * static_cast<int>(rank) + 8 * c : 512 + 32 * static_cast<int>(rank) + 8 * (c - 32);
-        const uint16_t* src = valid ? kv + static_cast<int64_t>(slot) * kDqk + off : kv;
-        const uint32_t dst = (c < 32) ? base + (c >> 3) * kLatBlock + n * 128 + (((c & 7) ^ (n & 7)) << 4)
-                                      : base + 4 * kLatBlock + n * 64 + (((c - 32) ^ ((n >> 1) & 3)) << 4);
-        cp_async16(dst, src, valid ? 16u : 0u);
+        for (int k = 0; k < kNk * 12 / kProducers; ++k) {
+          const int i = ptid + k * kProducers;
+          const int n = i / 12, c = 24 + i % 12;
+          const int s0 = __shfl_sync(0xffffffffu, cur0, n & 31), s1 = __shfl_sync(0xffffffffu, cur1, n & 31);
+          const int slot = n < 32 ? s0 : s1;
+          cp_async16(base + chunk_dst(n, c), kv + static_cast<int64_t>(slot) * kDqk + chunk_col(c), 16u);
+        }
+      } else {
+        // a masked key in the step: everything by cp.async, zero-filled where masked
+        if (warp == 1 && lane == 0) mbar_arrive(&sh.k_full[st]);
+#pragma unroll 4
+        for (int k = 0; k < kNk * 36 / kProducers; ++k) {
+          const int i = ptid + k * kProducers;
+          const int n = i / 36, c = i - n * 36;
+          const int s0 = __shfl_sync(0xffffffffu, cur0, n & 31), s1 = __shfl_sync(0xffffffffu, cur1, n & 31);
+          const int slot = n < 32 ? s0 : s1;
+          const bool valid = kbase + n < kend && in_pool(slot);
+          const uint16_t* src = valid ? kv + static_cast<int64_t>(slot) * kDqk + chunk_col(c) : kv;
+          cp_async16(base + chunk_dst(n, c), src, valid ? 16u : 0u);
+        }
       }
       cp_async_arrive_noinc(&sh.k_full[st]);
+      issued = j + 1;
       cur0 = nxt0;
       cur1 = nxt1;
     }
     cp_async_wait<0>();
   } else {
-    // ------------------------------------------------------------------ softmax + epilogue
-    const int r = tid - 128;
+    // ------------------------------------------------------------------ softmax sets + epilogue
+    const int set = (warp - 4) >> 2;                   // 0: even steps, 1: odd steps
+    const int r = (warp & 3) * 32 + lane;              // row of the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int grow = row_tile * kTileRows + r;
     const bool row_valid = grow < p.rows;
+    float* hand = reinterpret_cast<float*>(smem + kOffHand);   // [2][128]
+    float* fin = reinterpret_cast<float*>(smem + kOffFin);     // [2 sets][2][128]
 
-    // Q_r: latent dims [256 rank, +256) -> TMEM, rope dims [512 + 32 rank, +32) -> smem
+    // Q_r: latent dims [256 rank + 128 set, +128) -> TMEM, rope dims [512 + 32 rank, +32) -> smem
     {
       const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(b) * p.rows + grow) * kDqk);
       const uint4 zero = make_uint4(0, 0, 0, 0);
 #pragma unroll 1
-      for (int c0 = 0; c0 < 32; c0 += 8) {
+      for (int c0 = 0; c0 < 16; c0 += 8) {
         uint32_t v[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 x = row_valid ? __ldg(qsrc + 32 * rank + c0 + c) : zero;
+          const uint4 x = row_valid ? __ldg(qsrc + 32 * rank + 16 * set + c0 + c) : zero;
           v[4 * c] = x.x, v[4 * c + 1] = x.y, v[4 * c + 2] = x.z, v[4 * c + 3] = x.w;
         }
-        tmem_st32(tmem + lane_off + kColQ + c0 * 4, v);
+        tmem_st32(tmem + lane_off + kColQ + 64 * set + c0 * 4, v);
       }
+      if (set == 0) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 x = row_valid ? __ldg(qsrc + 64 + 4 * rank + c) : zero;
-        *reinterpret_cast<uint4*>(qrope + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = x;
+        for (int c = 0; c < 4; ++c) {
+          const uint4 x = row_valid ? __ldg(qsrc + 64 + 4 * rank + c) : zero;
+          *reinterpret_cast<uint4*>(qrope + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = x;
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -276,125 +348,132 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     }
 
     const uint32_t peer = rank ^ 1u;
-    uint32_t x_remote[2], e_remote[2], xbar_remote[2];
+    const uint32_t x_remote = mapa_shared(stage0 + kOffX, peer);
+    const uint32_t e_remote = mapa_shared(stage0 + kOffE, peer);
+    uint32_t xbar_remote[kXBufs];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      x_remote[i] = mapa_shared(smem_u32(xbuf + i * kXBytes), peer);
-      e_remote[i] = mapa_shared(smem_u32(ebuf + i * kEBytes), peer);
-      xbar_remote[i] = mapa_shared(smem_u32(&sh.x_full[i]), peer);
-    }
+    for (int i = 0; i < kXBufs; ++i) xbar_remote[i] = mapa_shared(smem_u32(&sh.x_full[i]), peer);
     const int32_t* slots = p.slot_idx + static_cast<int64_t>(b) * p.slot_stride;
     const uint32_t rsw = static_cast<uint32_t>(r & 7);
-    float m_used = -CUDART_INF_F, l = 0.f;
+    const bool lead = (warp & 3) == 0 && lane == 0;    // row 0 of this set
+    float m_used = -CUDART_INF_F;                      // running max after the last step seen
+    float m_ref = -CUDART_INF_F, l = 0.f;              // this set's row sum, relative to m_ref
     auto fetch_slot = [&](int j, int e) -> int {
       const int key = kbegin + j * kNk + lane + 32 * e;
       return key < kend ? __ldg(slots + key) : 0;
     };
-    // slots of this lane's two keys, fetched one step ahead
-    int sl0 = fetch_slot(0, 0), sl1 = fetch_slot(0, 1);
+    int sl0 = fetch_slot(set, 0), sl1 = fetch_slot(set, 1);
 
-    // Step t uses exchange buffer t % 2.  The peer writes step t only after it
-    // has received our step t-1, which we send after finishing step t-2, the
-    // last reader of that buffer.
-    for (int j = 0; ok && j < ntiles; ++j) {
+    // Step t uses exchange buffer t % 4.  The peer writes step t only after its
+    // step t-2 got our partial, which this set sends after finishing step t-4,
+    // the last reader of that buffer.
+    for (int j = set; ok && j < ntiles; j += 2) {
       const int sb = j % 2;
+      const int xb_i = j % kXBufs;
       const int kbase = kbegin + j * kNk;
       const int cur0 = sl0, cur1 = sl1;
-      if (j + 1 < ntiles) {
-        sl0 = fetch_slot(j + 1, 0);
-        sl1 = fetch_slot(j + 1, 1);
+      if (j + 2 < ntiles) {
+        sl0 = fetch_slot(j + 2, 0);
+        sl1 = fetch_slot(j + 2, 1);
       }
-      if (r == 0) mbar_arrive_expect_tx(&sh.x_full[sb], kXBytes + kEBytes);
+      if (lead) mbar_arrive_expect_tx(&sh.x_full[xb_i], kXBytes + kEBytes);
       if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.s_full[sb], (j / 2) & 1, abort))) { ok = false; break; }
       tc_fence_after();
       float x[64];
-      {
-        float t0[32], t1[32];
-        tmem_ld32(tmem + lane_off + kColS + sb * kNk, t0);
-        tmem_ld32(tmem + lane_off + kColS + sb * kNk + 32, t1);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          x[k] = t0[k] * p.scale_log2;
-          x[32 + k] = t1[k] * p.scale_log2;
-        }
-      }
+      tmem_ld32(tmem + lane_off + kColS + sb * kNk, *reinterpret_cast<float(*)[32]>(&x[0]));
+      tmem_ld32(tmem + lane_off + kColS + sb * kNk + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
       // encode own partial (block floating point), send it, and decode it again
       float amax = 0.f;
 #pragma unroll
       for (int k = 0; k < 64; ++k) amax = fmaxf(amax, fabsf(x[k]));
-      const int e = block_exponent(amax);
-      const float enc = pow2i(14 - e), dec = pow2i(e - 14);
+      const int e = block_exponent(amax * p.scale_log2);
+      const float enc = p.scale_log2 * pow2i(14 - e), dec = pow2i(e - 14), mdec = -kMagic * dec;
       {
-        const uint32_t xr = x_remote[sb] + r * 128, br = xbar_remote[sb];
+        const uint32_t xr = x_remote + xb_i * kXBytes + r * 128, br = xbar_remote[xb_i];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t w[4];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int k = 8 * c + 2 * h;
-            const int q0 = __float2int_rn(x[k] * enc), q1 = __float2int_rn(x[k + 1] * enc);
-            w[h] = (static_cast<uint32_t>(q0) & 0xffffu) | (static_cast<uint32_t>(q1) << 16);
-            x[k] = static_cast<float>(q0) * dec;
-            x[k + 1] = static_cast<float>(q1) * dec;
+          for (int q = 0; q < 4; ++q) {
+            const int k = 8 * c + 2 * q;
+            const float t0 = fmaf(x[k], enc, kMagic), t1 = fmaf(x[k + 1], enc, kMagic);
+            w[q] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
+            x[k] = fmaf(t0, dec, mdec);
+            x[k + 1] = fmaf(t1, dec, mdec);
           }
           st_async_v4(xr + ((c ^ rsw) << 4), make_uint4(w[0], w[1], w[2], w[3]), br);
         }
-        st_async_b32(e_remote[sb] + r * 4, static_cast<uint32_t>(e), br);
+        st_async_b32(e_remote + xb_i * kEBytes + r * 4, static_cast<uint32_t>(e), br);
       }
       // key mask of this step (past the split end or a slot outside the pool)
       const uint32_t masked0 = __ballot_sync(
           0xffffffffu, kbase + lane >= kend || cur0 < 0 || static_cast<int64_t>(cur0) >= p.pool_slots);
       const uint32_t masked1 = __ballot_sync(
           0xffffffffu, kbase + lane + 32 >= kend || cur1 < 0 || static_cast<int64_t>(cur1) >= p.pool_slots);
-      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_full[sb], (j / 2) & 1, abort, true))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_full[xb_i], (j / kXBufs) & 1, abort, true))) {
         ok = false;
         break;
       }
       // add the peer's partial: s = own + peer (fp32 addition commutes, so both CTAs agree)
       float mx = -CUDART_INF_F;
       {
-        const uint8_t* xb = xbuf + sb * kXBytes + r * 128;
-        const int pe = *reinterpret_cast<const int*>(ebuf + sb * kEBytes + r * 4);
-        const float pdec = pow2i(pe - 14);
+        const uint8_t* xbp = smem + kOffX + xb_i * kXBytes + r * 128;
+        const int pe = *reinterpret_cast<const int*>(smem + kOffE + xb_i * kEBytes + r * 4);
+        const float pdec = pow2i(pe - 14), pm = -kMagic * pdec;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xb + ((c ^ rsw) << 4));
+          const uint4 v = *reinterpret_cast<const uint4*>(xbp + ((c ^ rsw) << 4));
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int k = 8 * c + 2 * h;
-            const float a = static_cast<float>(static_cast<int>(static_cast<int16_t>(w[h] & 0xffffu))) * pdec;
-            const float bb = static_cast<float>(static_cast<int>(w[h]) >> 16) * pdec;
-            const uint32_t mk = k < 32 ? masked0 : masked1;
-            x[k] = ((mk >> (k & 31)) & 1u) ? -CUDART_INF_F : x[k] + a;
-            x[k + 1] = ((mk >> ((k + 1) & 31)) & 1u) ? -CUDART_INF_F : x[k + 1] + bb;
-            mx = fmaxf(mx, fmaxf(x[k], x[k + 1]));
+          for (int q = 0; q < 4; ++q) {
+            const int k = 8 * c + 2 * q;
+            const float a = fmaf(__uint_as_float(__byte_perm(w[q], kMagicHi, 0x7610)), pdec, pm);
+            const float bb = fmaf(__uint_as_float(__byte_perm(w[q], kMagicHi, 0x7632)), pdec, pm);
+            x[k] += a;
+            x[k + 1] += bb;
           }
+        }
+        if ((masked0 | masked1) != 0u) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (((k < 32 ? masked0 : masked1) >> (k & 31)) & 1u) x[k] = -CUDART_INF_F;
+        }
+#pragma unroll
+        for (int k = 0; k < 64; ++k) mx = fmaxf(mx, x[k]);
+      }
+      // running max after step j-1 comes from the other set
+      if (j > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.m_ready[(j - 1) % 2], ((j - 1) / 2) & 1, abort))) {
+          ok = false;
+          break;
+        }
+        m_used = hand[((j - 1) % 2) * kTileRows + r];
+      }
+      const float m_prev = m_used;
+      if (mx > m_used + kRescaleThreshold) m_used = mx;
+      hand[sb * kTileRows + r] = m_used;
+      mbar_arrive(&sh.m_ready[sb]);
+      const float alpha = (m_used == m_prev) ? 1.f : fast_exp2(m_prev - m_used);  // 0 on the first growth
+      if (__any_sync(0xffffffffu, alpha != 1.f) && j > 0) {
+        // O must hold every earlier step: wait for P.V of step j-1 (MMAs complete in order)
+        if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.pv_done[(j - 1) % 2], ((j - 1) / 2) & 1, abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          float o[32];
+          tmem_ld32(tmem + lane_off + kColO + c, o);
+          uint32_t ob[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ob[k] = __float_as_uint(o[k] * alpha);
+          tmem_st32(tmem + lane_off + kColO + c, ob);
         }
       }
-      const bool need = mx > m_used + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? mx : m_used;
-        const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
-        if (j > 0) {
-          // O must hold every earlier step: wait for P.V of step j-1 (MMAs complete in order)
-          if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.pv_done[(j - 1) % 2], ((j - 1) / 2) & 1, abort))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 256; c += 32) {
-            float o[32];
-            tmem_ld32(tmem + lane_off + kColO + c, o);
-            uint32_t ob[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) ob[k] = __float_as_uint(o[k] * alpha);
-            tmem_st32(tmem + lane_off + kColO + c, ob);
-          }
-        }
-        l *= alpha;
-        m_used = m_new;
+      if (m_used != m_ref) {
+        if (l > 0.f) l *= fast_exp2(m_ref - m_used);
+        m_ref = m_used;
       }
       const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
       float sum = 0.f;
@@ -411,25 +490,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       mbar_arrive(&sh.p_ready[sb]);
     }
 
-    // epilogue: wait for the last P.V, then o = O / l and lse = (m + log2 l) ln 2
+    // epilogue: combine both sets' row sums, wait for the last P.V, then
+    // o = O / l (set s writes O columns [128 s, 128 s + 128)) and lse.
+    fin[(set * 2 + 0) * kTileRows + r] = l;
+    fin[(set * 2 + 1) * kTileRows + r] = m_ref;
+    if (bar_red_or(kSoftmaxBarrier, 256, !ok)) ok = false;
+    const float l_o = fin[((set ^ 1) * 2 + 0) * kTileRows + r], m_o = fin[((set ^ 1) * 2 + 1) * kTileRows + r];
+    const float m_fin = fmaxf(m_ref, m_o);
+    const float lrow = (l > 0.f ? l * fast_exp2(m_ref - m_fin) : 0.f) + (l_o > 0.f ? l_o * fast_exp2(m_o - m_fin) : 0.f);
     if (ok && !mbar_wait_abortable(&sh.pv_done[(ntiles - 1) % 2], ((ntiles - 1) / 2) & 1, abort)) ok = false;
     tc_fence_after();
     if (__all_sync(0xffffffffu, ok)) {
       const int64_t prow = (static_cast<int64_t>(b) * p.max_splits + split) * (p.row_tiles * kTileRows) + grow;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float inv_l = lrow > 0.f ? 1.f / lrow : 0.f;
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 32) {
+      for (int c = 0; c < 128; c += 32) {
         float o[32];
-        tmem_ld32(tmem + lane_off + kColO + c, o);
+        tmem_ld32(tmem + lane_off + kColO + 128 * set + c, o);
         if (row_valid) {
-          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * kDv + 256 * rank + c);
+          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * kDv + 256 * rank + 128 * set + c);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             dst[k] = make_float4(o[4 * k] * inv_l, o[4 * k + 1] * inv_l, o[4 * k + 2] * inv_l, o[4 * k + 3] * inv_l);
         }
       }
-      if (rank == 0 && row_valid)
-        p.lse_part[prow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
+      if (rank == 0 && set == 0 && row_valid)
+        p.lse_part[prow] = lrow > 0.f ? (m_fin + log2f(lrow)) * kLn2 : -CUDART_INF_F;
     }
   }
 
@@ -439,6 +525,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
   }
   tc_fence_before();
   __syncthreads();
+  if (*abort && warp >= 1 && warp < 4 && lane == 0) {
+    // after a timeout, bulk copies of unconsumed stages may still be landing:
+    // wait for them (bounded) before the shared memory is released
+    for (int t = max(0, issued - kStages); t < issued; ++t) mbar_wait(&sh.k_full[t % kStages], (t / kStages) & 1, 1u << 20);
+  }
   cluster_sync();  // no CTA leaves while its peer may still write into its shared memory
   if (warp == 0) {
     tc_fence_after();

@@ -65,6 +65,19 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t pari
   return false;
 }
 
+// Named barrier over `count` threads that also ORs a predicate across them;
+// returns the OR.  Lets a group of warps leave a loop together.
+__device__ __forceinline__ bool bar_red_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- clusters / DSMEM
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -94,6 +107,26 @@ __device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, u
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr), "r"(v),
                "r"(remote_bar)
                : "memory");
+}
+
+// ---------------------------------------------------------------- TMA
+// 2-D tiled load of one box at coordinates (x, y) into shared memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// Four rows (row0..row3, all inside the tensor) of a 2-D tensor map at column x,
+// box = (box width) x 1 row each, stored consecutively with the map's swizzle.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int row0, int row1, int row2,
+                                            int row3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(row0), "r"(row1), "r"(row2), "r"(row3), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // ---------------------------------------------------------------- cp.async (16 B, zero fill)
