@@ -115,17 +115,18 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// The pool as a 2-D bf16 tensor [rows][576] (1152-byte rows), 128-byte swizzle,
-// box of 64 columns x box_rows rows.
-bool encode_pool_map(CUtensorMap* m, const void* pool, int64_t rows, uint32_t box_rows) {
+// The pool as a 2-D bf16 tensor [rows][576] (1152-byte rows), box of box_cols
+// columns x box_rows rows, 128-byte swizzle (64 columns) or 64-byte (32 columns).
+bool encode_pool_map(CUtensorMap* m, const void* pool, int64_t rows, uint32_t box_cols, uint32_t box_rows) {
   const EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
-  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t elem_strides[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, elem_strides,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -178,10 +179,11 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
     if (plan.splits > 0) {
       PrefixParams pp;
-      // the 64-row block map (contiguous steps) only when the pool has 64 rows
+      // the 64-row box maps (steps of consecutive slots) only when the pool has 64 rows
       pp.block_loads = dims->pool_slots >= kKeysPerTile ? 1 : 0;
-      if (!encode_pool_map(&pp.tmap_rows, kv_pool, dims->pool_slots, 1) ||
-          (pp.block_loads && !encode_pool_map(&pp.tmap_block, kv_pool, dims->pool_slots, kKeysPerTile)))
+      if (!encode_pool_map(&pp.tmap_rows, kv_pool, dims->pool_slots, 64, 1) ||
+          (pp.block_loads && (!encode_pool_map(&pp.tmap_block, kv_pool, dims->pool_slots, 64, kKeysPerTile) ||
+                              !encode_pool_map(&pp.tmap_rope, kv_pool, dims->pool_slots, 32, kKeysPerTile))))
         return DDT_ERR_LAUNCH;
       pp.q = static_cast<const uint16_t*>(q);
       pp.kv = static_cast<const uint16_t*>(kv_pool);

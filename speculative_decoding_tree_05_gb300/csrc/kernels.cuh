@@ -21,6 +21,7 @@ constexpr int32_t kStatusTimeout = 8;
 struct PrefixParams {
   CUtensorMap tmap_rows;     // kv_pool as [N rows][576 cols] bf16, box 64 cols x 1 row, 128-byte swizzle
   CUtensorMap tmap_block;    // same tensor, box 64 cols x 64 rows, 128-byte swizzle
+  CUtensorMap tmap_rope;     // same tensor, box 32 cols x 64 rows, 64-byte swizzle
   const uint16_t* q;         // bf16 [B, T, H, 576]
   const uint16_t* kv;        // bf16 [N, 576]
   const int32_t* slot_idx;   // [B, slot_stride]
@@ -33,7 +34,7 @@ struct PrefixParams {
   int32_t max_splits;        // split slots per request in the workspace
   int32_t max_prefix_len;
   float scale_log2;          // sm_scale * log2(e)
-  int32_t block_loads;       // tmap_block is valid (pool has >= 64 rows)
+  int32_t block_loads;       // tmap_block and tmap_rope are valid (pool has >= 64 rows)
   float* o_part;             // fp32 [B, max_splits, row_tiles*128, 512]
   float* lse_part;           // fp32 [B, max_splits, row_tiles*128], natural log
   int32_t* status;

@@ -20,6 +20,11 @@
 // O_r += P . V_r for its own 256 v dims.  Every gathered row is read once per
 // pair and no MMA work is duplicated.
 //
+// Each softmax set owns one exchange buffer in each CTA (step t uses buffer
+// t % 2); before writing step t the sender waits until the receiver has read
+// step t-2 from it (a barrier in the sender that the receiver's warps arrive on
+// remotely).
+//
 // Partial-score exchange format: per row and 64-key step, block floating point
 // -- one power-of-two exponent e with every |x| < 2^e and 64 int16 mantissas
 // round(x * 2^(14-e)), x being the partial score in log2 units.  That is half
@@ -36,7 +41,7 @@
 //               tcgen05.mma costs about 45 issue cycles whatever its shape, so
 //               each MMA is at least M=128 x N=64 (scores) or N=256 (P.V).
 //   warps 1-3   producers: load the CTA's dims of 64 slot rows per step into a
-//               3-stage ring, the step's slot indices fetched one step ahead.
+//               5-stage ring, the step's slot indices fetched one step ahead.
 //               A step whose 64 slots are consecutive (a compacted pool) is 5
 //               tiled TMA boxes of 64 rows.  A scattered step uses TMA
 //               tile::gather4 for latent blocks 0-2 (16 lanes of each producer
@@ -56,9 +61,10 @@
 //               when the running max grows by more than 8 (lazily); P (bf16)
 //               is written over its S buffer and read from TMEM by P.V.
 // TMEM columns: O_r [0,256), S buffers 2 x 64 at [256,384), Q_r latent [384,512).
-// Shared memory per stage: 4 latent blocks [64 keys][64 dims] + 1 rope block
-// [64 keys][64 rope dims] (128-byte swizzle, 8 KB each; CTA r reads rope dims
-// [32r, 32r+32) of it).
+// Shared memory per stage: 4 latent blocks [64 keys][64 dims] (128-byte
+// swizzle, 8 KB each) + the CTA's rope block [64 keys][32 dims] (64-byte
+// swizzle, 4 KB).  The stage's lifetime runs from its load through S, the
+// softmax with its exchange, and P.V, so the ring is as deep as fits.
 // The latent blocks are the K operand of S (K-major) and, read MN-major, the
 // V operand of P.V.
 #include <cuda_runtime.h>
@@ -71,12 +77,13 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kNk = kKeysPerTile;                        // 64 keys per step
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kLatBlock = kNk * 128;                     // 8192
-constexpr int kStageBytes = 5 * kLatBlock;               // 40960: 4 latent blocks + the rope block
+constexpr int kRopeBlock = kNk * 64;                     // 4096
+constexpr int kStageBytes = 4 * kLatBlock + kRopeBlock;  // 36864
 constexpr int kProducers = 96;
 constexpr int kGatherBlocks = 3;                         // latent blocks fetched by gather4 on scattered steps
-constexpr int kXBufs = 4;                                // exchange buffers (step t uses t % 4)
+constexpr int kXBufs = 2;                                // exchange buffers (step t uses t % 2)
 constexpr int kXBytes = kTileRows * kNk * 2;             // 16384: int16 mantissas of one step
 constexpr int kEBytes = kTileRows * 4;                   // 512: one exponent per row
 constexpr int kQRopeBytes = kTileRows * 64;              // 8192: Q_r rope dims, 64-byte swizzle
@@ -101,7 +108,8 @@ struct Shared {
   uint64_t k_empty[kStages];  // MMA -> producers: stage consumed (after P.V)
   uint64_t s_full[2];         // MMA -> softmax set t%2: partial scores of step t in S buffer t % 2
   uint64_t p_ready[2];        // softmax set -> MMA: P of step t in S buffer t % 2, O rescaled
-  uint64_t x_full[kXBufs];    // peer -> softmax: peer's partial scores of step t in buffer t % 4
+  uint64_t x_full[kXBufs];    // peer -> softmax: peer's partial scores of step t in buffer t % 2
+  uint64_t x_free[kXBufs];    // peer's softmax warps -> sender: step t read from the peer's buffer t % 2
   uint64_t pv_done[2];        // MMA -> softmax: P.V of step t completes phase t/2 of pv_done[t%2]
   uint64_t m_ready[2];        // softmax set -> other set: running max after step t in hand[t % 2]
   uint64_t q_ready;           // softmax -> MMA: Q_r staged
@@ -154,7 +162,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       mbar_init(&sh.pv_done[i], 1);
       mbar_init(&sh.m_ready[i], 128);
     }
-    for (int i = 0; i < kXBufs; ++i) mbar_init(&sh.x_full[i], 1);
+    for (int i = 0; i < kXBufs; ++i) {
+      mbar_init(&sh.x_full[i], 1);
+      mbar_init(&sh.x_free[i], 4);  // the 4 warps of the peer's set
+    }
     mbar_init(&sh.q_ready, 256);
     sh.abort = 0;
     fence_mbar_init();
@@ -195,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
           const uint64_t ad = smem_desc(qrope_s + ks * 32, 16, 512, kSwizzle64B);
-          const uint64_t bd = smem_desc(base + 4 * kLatBlock + 64 * rank + ks * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(base + 4 * kLatBlock + ks * 32, 16, 512, kSwizzle64B);
           mma_ss(sb, ad, bd, kIdescS, 1u);
         }
         mma_commit(&sh.s_full[t % 2]);
@@ -230,11 +241,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       return key < kend ? __ldg(slots + key) : -1;
     };
     auto in_pool = [&](int s_) { return s_ >= 0 && static_cast<int64_t>(s_) < p.pool_slots; };
-    // 16-byte chunk c of the CTA's 48 per row -> (source column, smem offset in the stage):
-    // c < 32 latent block c/8, c >= 32 the CTA's rope chunks in the rope block
+    // 16-byte chunk c of the CTA's 36 per row -> (source column, smem offset in the stage):
+    // c < 32 latent block c/8 (128-byte swizzle), c >= 32 the rope block (64-byte swizzle)
     auto chunk_dst = [&](int n, int c) -> uint32_t {
       return c < 32 ? (c >> 3) * kLatBlock + n * 128 + (((c & 7) ^ (n & 7)) << 4)
-                    : 4 * kLatBlock + n * 128 + (((4 * rk + c - 32) ^ (n & 7)) << 4);
+                    : 4 * kLatBlock + n * 64 + (((c - 32) ^ ((n >> 1) & 3)) << 4);
     };
     auto chunk_col = [&](int c) -> int { return c < 32 ? 256 * rk + 8 * c : 512 + 32 * rk + 8 * (c - 32); };
     int cur0 = fetch(0, 0), cur1 = fetch(0, 1);
@@ -260,12 +271,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
           p.block_loads && all_valid && __all_sync(0xffffffffu, cur0 == first + lane && cur1 == first + 32 + lane);
       const uint32_t base = stage0 + st * kStageBytes;
       if (contiguous) {
-        // 64 consecutive rows: five 64-row boxes (all latent blocks and the rope block)
+        // 64 consecutive rows: five 64-row boxes (the latent blocks and the rope block)
         if (warp == 1 && lane == 0) {
           mbar_arrive_expect_tx(&sh.k_full[st], kStageBytes);
 #pragma unroll
-          for (int c = 0; c < 5; ++c)
-            tma_load_2d(base + c * kLatBlock, &p.tmap_block, c < 4 ? 256 * rk + 64 * c : 512, first, &sh.k_full[st]);
+          for (int c = 0; c < 4; ++c)
+            tma_load_2d(base + c * kLatBlock, &p.tmap_block, 256 * rk + 64 * c, first, &sh.k_full[st]);
+          tma_load_2d(base + 4 * kLatBlock, &p.tmap_rope, 512 + 32 * rk, first, &sh.k_full[st]);
         }
       } else if (all_valid) {
         // gather4 for latent blocks 0..2 (producer warp w takes block w-1) ...
@@ -350,11 +362,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     const uint32_t peer = rank ^ 1u;
     const uint32_t x_remote = mapa_shared(stage0 + kOffX, peer);
     const uint32_t e_remote = mapa_shared(stage0 + kOffE, peer);
-    uint32_t xbar_remote[kXBufs];
+    uint32_t xbar_remote[kXBufs], xfree_remote[kXBufs];
 #pragma unroll
-    for (int i = 0; i < kXBufs; ++i) xbar_remote[i] = mapa_shared(smem_u32(&sh.x_full[i]), peer);
+    for (int i = 0; i < kXBufs; ++i) {
+      xbar_remote[i] = mapa_shared(smem_u32(&sh.x_full[i]), peer);
+      xfree_remote[i] = mapa_shared(smem_u32(&sh.x_free[i]), peer);
+    }
     const int32_t* slots = p.slot_idx + static_cast<int64_t>(b) * p.slot_stride;
-    const uint32_t rsw = static_cast<uint32_t>(r & 7);
     const bool lead = (warp & 3) == 0 && lane == 0;    // row 0 of this set
     float m_used = -CUDART_INF_F;                      // running max after the last step seen
     float m_ref = -CUDART_INF_F, l = 0.f;              // this set's row sum, relative to m_ref
@@ -364,9 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     };
     int sl0 = fetch_slot(set, 0), sl1 = fetch_slot(set, 1);
 
-    // Step t uses exchange buffer t % 4.  The peer writes step t only after its
-    // step t-2 got our partial, which this set sends after finishing step t-4,
-    // the last reader of that buffer.
+    // Step t uses exchange buffer t % 2 (this set's) in both CTAs.
     for (int j = set; ok && j < ntiles; j += 2) {
       const int sb = j % 2;
       const int xb_i = j % kXBufs;
@@ -388,8 +400,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       for (int k = 0; k < 64; ++k) amax = fmaxf(amax, fabsf(x[k]));
       const int e = block_exponent(amax * p.scale_log2);
       const float enc = p.scale_log2 * pow2i(14 - e), dec = pow2i(e - 14), mdec = -kMagic * dec;
+      // the peer must have read step j-2 out of the buffer before it is overwritten
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_free[xb_i], ((j - 2) / 2) & 1, abort, true))) {
+        ok = false;
+        break;
+      }
       {
-        const uint32_t xr = x_remote + xb_i * kXBytes + r * 128, br = xbar_remote[xb_i];
+        // chunk-major buffer [8 chunks][128 rows][16 B]: a warp's store of one chunk is 512 contiguous bytes
+        const uint32_t xr = x_remote + xb_i * kXBytes + r * 16, br = xbar_remote[xb_i];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t w[4];
@@ -401,7 +419,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
             x[k] = fmaf(t0, dec, mdec);
             x[k + 1] = fmaf(t1, dec, mdec);
           }
-          st_async_v4(xr + ((c ^ rsw) << 4), make_uint4(w[0], w[1], w[2], w[3]), br);
+          st_async_v4(xr + c * (kTileRows * 16), make_uint4(w[0], w[1], w[2], w[3]), br);
         }
         st_async_b32(e_remote + xb_i * kEBytes + r * 4, static_cast<uint32_t>(e), br);
       }
@@ -417,12 +435,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       // add the peer's partial: s = own + peer (fp32 addition commutes, so both CTAs agree)
       float mx = -CUDART_INF_F;
       {
-        const uint8_t* xbp = smem + kOffX + xb_i * kXBytes + r * 128;
+        const uint8_t* xbp = smem + kOffX + xb_i * kXBytes + r * 16;
         const int pe = *reinterpret_cast<const int*>(smem + kOffE + xb_i * kEBytes + r * 4);
         const float pdec = pow2i(pe - 14), pm = -kMagic * pdec;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xbp + ((c ^ rsw) << 4));
+          const uint4 v = *reinterpret_cast<const uint4*>(xbp + c * (kTileRows * 16));
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -433,6 +451,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
             x[k + 1] += bb;
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(xfree_remote[xb_i]);  // this warp's rows of the buffer are read
         if ((masked0 | masked1) != 0u) {
 #pragma unroll
           for (int k = 0; k < 64; ++k)
