@@ -40,6 +40,10 @@
 //   warp 0      TMEM allocation; lane 0 issues every tcgen05.mma.  A
 //               tcgen05.mma costs about 45 issue cycles whatever its shape, so
 //               each MMA is at least M=128 x N=64 (scores) or N=256 (P.V).
+//               The issuer polls its barriers and issues whichever is ready:
+//               S of the next step (its stage loaded and the one S buffer
+//               read out by the softmax) or P.V of the oldest step whose P
+//               is written, so scores run ahead of the softmax and exchange.
 //   warps 1-3   producers: load the CTA's dims of 64 slot rows per step into a
 //               5-stage ring, the step's slot indices fetched one step ahead.
 //               A step whose 64 slots are consecutive (a compacted pool) is 5
@@ -58,9 +62,11 @@
 //               running max of every row (step t waits for step t-1's); each
 //               set keeps its own row sums against the max it last used and
 //               the two are combined at the end.  O is rescaled in TMEM only
-//               when the running max grows by more than 8 (lazily); P (bf16)
-//               is written over its S buffer and read from TMEM by P.V.
-// TMEM columns: O_r [0,256), S buffers 2 x 64 at [256,384), Q_r latent [384,512).
+//               when the running max grows by more than 8 (lazily).  A set
+//               frees the S buffer as soon as it has loaded S into registers
+//               and writes P (bf16) into P buffer t % 2, read from TMEM by P.V.
+// TMEM columns: O_r [0,256), S [256,320), P buffers 2 x 32 at [320,384),
+// Q_r latent [384,512).
 // Shared memory per stage: 4 latent blocks [64 keys][64 dims] (128-byte
 // swizzle, 8 KB each) + the CTA's rope block [64 keys][32 dims] (64-byte
 // swizzle, 4 KB).  The stage's lifetime runs from its load through S, the
@@ -93,7 +99,7 @@ constexpr int kOffQRope = kOffE + kXBufs * kEBytes;
 constexpr int kOffHand = kOffQRope + kQRopeBytes;        // [2][128] running max handed between sets
 constexpr int kOffFin = kOffHand + 2 * kTileRows * 4;    // [2 sets][2 (l, m)][128] final row state
 constexpr int kSmem = kOffFin + 2 * 2 * kTileRows * 4 + 1024;
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384, kTmemCols = 512;
+constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 384, kTmemCols = 512;
 constexpr uint32_t kIdescS = idesc_bf16_f32(kTileRows, kNk, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileRows, 256, false, true);
 constexpr float kRescaleThreshold = 8.f;                 // log2 units
@@ -106,8 +112,9 @@ static_assert(kNk == 64, "the step layout assumes 64 keys");
 struct Shared {
   uint64_t k_full[kStages];   // producers -> MMA: stage loaded
   uint64_t k_empty[kStages];  // MMA -> producers: stage consumed (after P.V)
-  uint64_t s_full[2];         // MMA -> softmax set t%2: partial scores of step t in S buffer t % 2
-  uint64_t p_ready[2];        // softmax set -> MMA: P of step t in S buffer t % 2, O rescaled
+  uint64_t s_full[2];         // MMA -> softmax set t%2: partial scores of step t in the S buffer
+  uint64_t s_free[2];         // softmax set t%2 -> MMA: S of step t loaded into registers
+  uint64_t p_ready[2];        // softmax set -> MMA: P of step t in P buffer t % 2, O rescaled
   uint64_t x_full[kXBufs];    // peer -> softmax: peer's partial scores of step t in buffer t % 2
   uint64_t x_free[kXBufs];    // peer's softmax warps -> sender: step t read from the peer's buffer t % 2
   uint64_t pv_done[2];        // MMA -> softmax: P.V of step t completes phase t/2 of pv_done[t%2]
@@ -158,6 +165,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.s_free[i], 128);
       mbar_init(&sh.p_ready[i], 128);
       mbar_init(&sh.pv_done[i], 1);
       mbar_init(&sh.m_ready[i], 128);
@@ -183,49 +191,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 
   if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer
-    // Tensor-core order: S_0, S_1, PV_0, S_2, PV_1, ...  S_{j+1} reuses the S
-    // buffer of step j-1, whose P was read by PV_{j-1}, issued just before.
     if (lane == 0) {
       if (!mbar_wait_abortable(&sh.q_ready, 0, abort)) ok = false;
       fence_proxy_async_smem();  // Q rope dims were stored to shared memory by the softmax threads
       tc_fence_after();
-      auto issue_s = [&](int t) -> bool {
-        const int st = t % kStages;
-        if (!mbar_wait_abortable(&sh.k_full[st], (t / kStages) & 1, abort)) return false;
-        // the stage was written by cp.async (generic proxy): order it before the
-        // tensor core's async-proxy reads
-        fence_proxy_async_smem();
-        tc_fence_after();
-        const uint32_t base = stage0 + st * kStageBytes;
-        const uint32_t sb = tmem + kColS + (t % 2) * kNk;
+      int ns = 0, np = 0;        // next step whose S / P.V is to be issued
+      uint32_t idle = 0;
+      while (ok && np < ntiles) {
+        bool progressed = false;
+        // S(ns): stage loaded, and S(ns-1) read out of the S buffer
+        if (ns < ntiles && mbar_test_wait(&sh.k_full[ns % kStages], (ns / kStages) & 1) &&
+            (ns == 0 || mbar_test_wait(&sh.s_free[(ns - 1) % 2], ((ns - 1) / 2) & 1))) {
+          // the stage may have been written by cp.async (generic proxy): order it
+          // before the tensor core's async-proxy reads
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t base = stage0 + (ns % kStages) * kStageBytes;
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-          const uint64_t bd = smem_desc(base + (ks >> 2) * kLatBlock + (ks & 3) * 32, 16, 1024, kSwizzle128B);
-          mma_ts(sb, tmem + kColQ + ks * 8, bd, kIdescS, ks > 0 ? 1u : 0u);
-        }
+          for (int ks = 0; ks < 16; ++ks) {
+            const uint64_t bd = smem_desc(base + (ks >> 2) * kLatBlock + (ks & 3) * 32, 16, 1024, kSwizzle128B);
+            mma_ts(tmem + kColS, tmem + kColQ + ks * 8, bd, kIdescS, ks > 0 ? 1u : 0u);
+          }
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const uint64_t ad = smem_desc(qrope_s + ks * 32, 16, 512, kSwizzle64B);
-          const uint64_t bd = smem_desc(base + 4 * kLatBlock + ks * 32, 16, 512, kSwizzle64B);
-          mma_ss(sb, ad, bd, kIdescS, 1u);
+          for (int ks = 0; ks < 2; ++ks) {
+            const uint64_t ad = smem_desc(qrope_s + ks * 32, 16, 512, kSwizzle64B);
+            const uint64_t bd = smem_desc(base + 4 * kLatBlock + ks * 32, 16, 512, kSwizzle64B);
+            mma_ss(tmem + kColS, ad, bd, kIdescS, 1u);
+          }
+          mma_commit(&sh.s_full[ns % 2]);
+          ++ns;
+          progressed = true;
         }
-        mma_commit(&sh.s_full[t % 2]);
-        return true;
-      };
-      if (ok && !issue_s(0)) ok = false;
-      for (int j = 0; ok && j < ntiles; ++j) {
-        if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
-        if (!mbar_wait_abortable(&sh.p_ready[j % 2], (j / 2) & 1, abort)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t base = stage0 + (j % kStages) * kStageBytes;
-        const uint32_t pb = tmem + kColS + (j % 2) * kNk;
+        // P.V(np): P written (and O rescaled) by its softmax set
+        if (np < ns && mbar_test_wait(&sh.p_ready[np % 2], (np / 2) & 1)) {
+          tc_fence_after();
+          const uint32_t base = stage0 + (np % kStages) * kStageBytes;
+          const uint32_t pb = tmem + kColP + (np % 2) * (kNk / 2);
 #pragma unroll
-        for (int ks = 0; ks < kNk / 16; ++ks) {
-          const uint64_t bd = smem_desc(base + ks * 16 * 128, kLatBlock, 1024, kSwizzle128B);
-          mma_ts(tmem + kColO, pb + ks * 8, bd, kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < kNk / 16; ++ks) {
+            const uint64_t bd = smem_desc(base + ks * 16 * 128, kLatBlock, 1024, kSwizzle128B);
+            mma_ts(tmem + kColO, pb + ks * 8, bd, kIdescPV, (np > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(&sh.k_empty[np % kStages]);
+          mma_commit(&sh.pv_done[np % 2]);
+          ++np;
+          progressed = true;
         }
-        mma_commit(&sh.k_empty[j % kStages]);
-        mma_commit(&sh.pv_done[j % 2]);
+        if (progressed) {
+          idle = 0;
+        } else if (++idle > (1u << 26) || ((idle & 255) == 255 && *abort)) {
+          ok = false;
+        }
       }
     }
     __syncwarp();
@@ -392,8 +408,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.s_full[sb], (j / 2) & 1, abort))) { ok = false; break; }
       tc_fence_after();
       float x[64];
-      tmem_ld32(tmem + lane_off + kColS + sb * kNk, *reinterpret_cast<float(*)[32]>(&x[0]));
-      tmem_ld32(tmem + lane_off + kColS + sb * kNk + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+      tmem_ld32(tmem + lane_off + kColS, *reinterpret_cast<float(*)[32]>(&x[0]));
+      tmem_ld32(tmem + lane_off + kColS + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+      tc_fence_before();
+      mbar_arrive(&sh.s_free[sb]);  // the S buffer may take the next step's scores
       // encode own partial (block floating point), send it, and decode it again
       float amax = 0.f;
 #pragma unroll
@@ -505,7 +523,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         pk[k] = pack_bf16x2(p0, p1);
       }
       l += sum;
-      tmem_st32(tmem + lane_off + kColS + sb * kNk, pk);
+      // P buffer sb was last read by P.V of step j-2
+      if (j >= 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.pv_done[sb], ((j - 2) / 2) & 1, abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st32(tmem + lane_off + kColP + sb * (kNk / 2), pk);
       tc_fence_before();
       mbar_arrive(&sh.p_ready[sb]);
     }
