@@ -32,9 +32,12 @@
 // at most 2^-15 * 2^e, i.e. 2^-14 of the row's largest partial in the step.
 // Rounding to an integer and packing use the float adder: x * 2^(14-e) + M with
 // M = 1.5 * 2^23 + 2^15 is an integer-valued float whose low 16 bits are the
-// biased mantissa, so no int/float conversion instruction is needed.  Both CTAs
-// decode both halves the same way and add them in the same order, so they hold
-// bit-identical scores and make identical softmax decisions.
+// biased mantissa, so no int/float conversion instruction is needed.  Each CTA
+// adds the peer's decoded partial to its own unrounded one, so the two CTAs'
+// scores differ by that rounding alone; each CTA keeps its own running max and
+// row sum and normalises its own half of O by them, so neither half depends on
+// the other CTA's softmax decisions (rank 0's log-sum-exp serves both halves in
+// the split merge, off by the same rounding).
 //
 // Per CTA (384 threads):
 //   warp 0      TMEM allocation; lane 0 issues every tcgen05.mma.  A
@@ -412,12 +415,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       tmem_ld32(tmem + lane_off + kColS + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
       tc_fence_before();
       mbar_arrive(&sh.s_free[sb]);  // the S buffer may take the next step's scores
-      // encode own partial (block floating point), send it, and decode it again
-      float amax = 0.f;
+      // encode own partial (block floating point) and send it; the own partial stays unrounded
+      float am[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains: a 64-long max chain is latency-bound
 #pragma unroll
-      for (int k = 0; k < 64; ++k) amax = fmaxf(amax, fabsf(x[k]));
-      const int e = block_exponent(amax * p.scale_log2);
-      const float enc = p.scale_log2 * pow2i(14 - e), dec = pow2i(e - 14), mdec = -kMagic * dec;
+      for (int k = 0; k < 64; ++k) am[k & 3] = fmaxf(am[k & 3], fabsf(x[k]));
+      const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
+      const float sl2 = p.scale_log2;
+      const int e = block_exponent(amax * sl2);
+      const float enc = sl2 * pow2i(14 - e);
       // the peer must have read step j-2 out of the buffer before it is overwritten
       if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_free[xb_i], ((j - 2) / 2) & 1, abort, true))) {
         ok = false;
@@ -434,8 +439,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
             const int k = 8 * c + 2 * q;
             const float t0 = fmaf(x[k], enc, kMagic), t1 = fmaf(x[k + 1], enc, kMagic);
             w[q] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
-            x[k] = fmaf(t0, dec, mdec);
-            x[k + 1] = fmaf(t1, dec, mdec);
           }
           st_async_v4(xr + c * (kTileRows * 16), make_uint4(w[0], w[1], w[2], w[3]), br);
         }
@@ -450,7 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         ok = false;
         break;
       }
-      // add the peer's partial: s = own + peer (fp32 addition commutes, so both CTAs agree)
+      // s = own * scale_log2 + peer (log2 units)
       float mx = -CUDART_INF_F;
       {
         const uint8_t* xbp = smem + kOffX + xb_i * kXBytes + r * 16;
@@ -465,8 +468,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
             const int k = 8 * c + 2 * q;
             const float a = fmaf(__uint_as_float(__byte_perm(w[q], kMagicHi, 0x7610)), pdec, pm);
             const float bb = fmaf(__uint_as_float(__byte_perm(w[q], kMagicHi, 0x7632)), pdec, pm);
-            x[k] += a;
-            x[k + 1] += bb;
+            x[k] = fmaf(x[k], sl2, a);
+            x[k + 1] = fmaf(x[k + 1], sl2, bb);
           }
         }
         __syncwarp();
@@ -476,8 +479,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
           for (int k = 0; k < 64; ++k)
             if (((k < 32 ? masked0 : masked1) >> (k & 31)) & 1u) x[k] = -CUDART_INF_F;
         }
+        float mq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-        for (int k = 0; k < 64; ++k) mx = fmaxf(mx, x[k]);
+        for (int k = 0; k < 64; ++k) mq[k & 3] = fmaxf(mq[k & 3], x[k]);
+        mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       }
       // running max after step j-1 comes from the other set
       if (j > 0) {
@@ -514,15 +519,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         m_ref = m_used;
       }
       const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
-      float sum = 0.f;
+      float sq[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const float p0 = fast_exp2(x[2 * k] - msub), p1 = fast_exp2(x[2 * k + 1] - msub);
-        sum += p0 + p1;
+        sq[k & 3] += p0 + p1;
         pk[k] = pack_bf16x2(p0, p1);
       }
-      l += sum;
+      l += (sq[0] + sq[1]) + (sq[2] + sq[3]);
       // P buffer sb was last read by P.V of step j-2
       if (j >= 2) {
         if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.pv_done[sb], ((j - 2) / 2) & 1, abort))) {
