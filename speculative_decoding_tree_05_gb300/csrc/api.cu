@@ -65,22 +65,25 @@ int make_plan(const ddt_dims* d, int sm_count, Plan* plan) {
   p.row_tiles = (p.rows + kTileRows - 1) / kTileRows;
   const int64_t L = d->max_prefix_len;
   if (L > 0 && d->batch > 0) {
-    // Pick the number of key splits that fills the GPU's CTA pairs in whole
-    // waves (each unit = one pair on one (request, row tile, split)); among
-    // equally good choices take the fewest splits.  Splits are at least
-    // kMinChunk keys long so per-unit set-up stays small.
+    // Pick the number of key splits s (each unit = one CTA pair on one
+    // (request, row tile, split)) that minimises the modelled time
+    //   waves(s) * (64-key steps per unit + kUnitOverheadSteps),
+    // the overhead being a unit's fixed cost (pipeline fill, Q staging, the
+    // write of its partial O) in step equivalents; among equal costs take the
+    // fewest splits.  Splits are at least kMinChunk keys long.
     const int64_t pairs = sm_count >= 2 ? sm_count / 2 : 1;
     const int64_t per_split = int64_t(d->batch) * p.row_tiles;
     const int64_t tiles = (L + kKeysPerTile - 1) / kKeysPerTile;
     const int64_t max_splits = std::max<int64_t>(1, std::min<int64_t>(64, (L + kMinChunk - 1) / kMinChunk));
     int64_t best = 1;
-    double best_eff = -1.0;
+    int64_t best_cost = -1;
     for (int64_t s = 1; s <= max_splits; ++s) {
-      const int64_t units = per_split * s;
-      const int64_t waves = (units + pairs - 1) / pairs;
-      const double eff = double(units) / double(waves * pairs);
-      if (eff > best_eff + 1e-9) {
-        best_eff = eff;
+      const int64_t steps = (tiles + s - 1) / s;            // per unit
+      const int64_t splits = (tiles + steps - 1) / steps;   // splits that actually hold keys
+      const int64_t waves = (per_split * splits + pairs - 1) / pairs;
+      const int64_t cost = waves * (steps + kUnitOverheadSteps);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
         best = s;
       }
     }

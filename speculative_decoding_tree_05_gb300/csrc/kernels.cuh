@@ -80,6 +80,7 @@ struct CompactParams {
 constexpr int kTileRows = 128;            // query rows per CTA pair (tcgen05 M)
 constexpr int kKeysPerTile = 64;          // keys per pipeline step
 constexpr int kMinChunk = 256;            // shortest key split the planner makes
+constexpr int kUnitOverheadSteps = 6;     // fixed cost of one prefix unit, in 64-key steps (measured)
 
 // Per-device set-up (shared-memory opt-in), called once per device before launches.
 cudaError_t configure_prefix();
