@@ -198,6 +198,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       if (!mbar_wait_abortable(&sh.q_ready, 0, abort)) ok = false;
       fence_proxy_async_smem();  // Q rope dims were stored to shared memory by the softmax threads
       tc_fence_after();
+      // operand descriptors of stage 0, built once; a stage or k-step is an offset
+      // (the issuing thread is serial and each MMA issue waits for the pipe, so
+      // rebuilding descriptors between MMAs would stretch every MMA)
+      const uint64_t d_lat = smem_desc(stage0, 16, 1024, kSwizzle128B);             // K of S: K-major
+      const uint64_t d_rope = smem_desc(stage0 + 4 * kLatBlock, 16, 512, kSwizzle64B);
+      const uint64_t d_qrope = smem_desc(qrope_s, 16, 512, kSwizzle64B);
+      const uint64_t d_v = smem_desc(stage0, kLatBlock, 1024, kSwizzle128B);         // V of P.V: MN-major
       int ns = 0, np = 0;        // next step whose S / P.V is to be issued
       uint32_t idle = 0;
       while (ok && np < ntiles) {
@@ -209,18 +216,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
           // before the tensor core's async-proxy reads
           fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t base = stage0 + (ns % kStages) * kStageBytes;
+          const uint32_t so = (ns % kStages) * kStageBytes;
+          const uint64_t dl = desc_advance(d_lat, so), dr = desc_advance(d_rope, so);
 #pragma unroll
-          for (int ks = 0; ks < 16; ++ks) {
-            const uint64_t bd = smem_desc(base + (ks >> 2) * kLatBlock + (ks & 3) * 32, 16, 1024, kSwizzle128B);
-            mma_ts(tmem + kColS, tmem + kColQ + ks * 8, bd, kIdescS, ks > 0 ? 1u : 0u);
-          }
+          for (int ks = 0; ks < 16; ++ks)
+            mma_ts(tmem + kColS, tmem + kColQ + ks * 8, desc_advance(dl, (ks >> 2) * kLatBlock + (ks & 3) * 32), kIdescS,
+                   ks > 0 ? 1u : 0u);
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint64_t ad = smem_desc(qrope_s + ks * 32, 16, 512, kSwizzle64B);
-            const uint64_t bd = smem_desc(base + 4 * kLatBlock + ks * 32, 16, 512, kSwizzle64B);
-            mma_ss(tmem + kColS, ad, bd, kIdescS, 1u);
-          }
+          for (int ks = 0; ks < 2; ++ks)
+            mma_ss(tmem + kColS, desc_advance(d_qrope, ks * 32), desc_advance(dr, ks * 32), kIdescS, 1u);
           mma_commit(&sh.s_full[ns % 2]);
           ++ns;
           progressed = true;
@@ -228,13 +232,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         // P.V(np): P written (and O rescaled) by its softmax set
         if (np < ns && mbar_test_wait(&sh.p_ready[np % 2], (np / 2) & 1)) {
           tc_fence_after();
-          const uint32_t base = stage0 + (np % kStages) * kStageBytes;
+          const uint64_t dv = desc_advance(d_v, (np % kStages) * kStageBytes);
           const uint32_t pb = tmem + kColP + (np % 2) * (kNk / 2);
 #pragma unroll
-          for (int ks = 0; ks < kNk / 16; ++ks) {
-            const uint64_t bd = smem_desc(base + ks * 16 * 128, kLatBlock, 1024, kSwizzle128B);
-            mma_ts(tmem + kColO, pb + ks * 8, bd, kIdescPV, (np > 0 || ks > 0) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < kNk / 16; ++ks)
+            mma_ts(tmem + kColO, pb + ks * 8, desc_advance(dv, ks * 16 * 128), kIdescPV, (np > 0 || ks > 0) ? 1u : 0u);
           mma_commit(&sh.k_empty[np % kStages]);
           mma_commit(&sh.pv_done[np % 2]);
           ++np;

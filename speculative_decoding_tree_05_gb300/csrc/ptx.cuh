@@ -246,6 +246,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
+// The same descriptor for an operand byte_off further on in shared memory: the
+// start-address field holds addr >> 4 in 14 bits, and shared addresses stay
+// below 256 KB, so the offset adds without a carry into the next field.  Lets an
+// MMA issuer build each descriptor once and step it with one add per MMA.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t byte_off) {
+  return desc + static_cast<uint64_t>(byte_off >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulator.
 // a_mn / b_mn select the MN-major (transposed) operand layout.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
