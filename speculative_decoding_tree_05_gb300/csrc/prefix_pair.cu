@@ -114,13 +114,13 @@ static_assert(kNk == 64, "the step layout assumes 64 keys");
 
 struct Shared {
   uint64_t k_full[kStages];   // producers -> MMA: stage loaded
-  uint64_t k_empty[kStages];  // MMA -> producers: stage consumed (after P.V)
+  uint64_t k_empty[kStages];  // MMA -> producers and softmax: P.V of step t done, its stage free
+                              // (phase t / kStages of k_empty[t % kStages])
   uint64_t s_full[2];         // MMA -> softmax set t%2: partial scores of step t in the S buffer
   uint64_t s_free[2];         // softmax set t%2 -> MMA: S of step t loaded into registers
   uint64_t p_ready[2];        // softmax set -> MMA: P of step t in P buffer t % 2, O rescaled
   uint64_t x_full[kXBufs];    // peer -> softmax: peer's partial scores of step t in buffer t % 2
   uint64_t x_free[kXBufs];    // peer's softmax warps -> sender: step t read from the peer's buffer t % 2
-  uint64_t pv_done[2];        // MMA -> softmax: P.V of step t completes phase t/2 of pv_done[t%2]
   uint64_t m_ready[2];        // softmax set -> other set: running max after step t in hand[t % 2]
   uint64_t q_ready;           // softmax -> MMA: Q_r staged
   uint32_t tmem_base;
@@ -170,7 +170,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.s_free[i], 128);
       mbar_init(&sh.p_ready[i], 128);
-      mbar_init(&sh.pv_done[i], 1);
       mbar_init(&sh.m_ready[i], 128);
     }
     for (int i = 0; i < kXBufs; ++i) {
@@ -237,8 +236,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 #pragma unroll
           for (int ks = 0; ks < kNk / 16; ++ks)
             mma_ts(tmem + kColO, pb + ks * 8, desc_advance(dv, ks * 16 * 128), kIdescPV, (np > 0 || ks > 0) ? 1u : 0u);
+          // one commit per MMA group: k_empty[stage] also tells the softmax that
+          // P.V(np) is done (a second commit straight after a first cannot be
+          // relied on to wait for the same MMAs)
           mma_commit(&sh.k_empty[np % kStages]);
-          mma_commit(&sh.pv_done[np % 2]);
           ++np;
           progressed = true;
         }
@@ -501,7 +502,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       const float alpha = (m_used == m_prev) ? 1.f : fast_exp2(m_prev - m_used);  // 0 on the first growth
       if (__any_sync(0xffffffffu, alpha != 1.f) && j > 0) {
         // O must hold every earlier step: wait for P.V of step j-1 (MMAs complete in order)
-        if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.pv_done[(j - 1) % 2], ((j - 1) / 2) & 1, abort))) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_abortable(&sh.k_empty[(j - 1) % kStages], ((j - 1) / kStages) & 1, abort))) {
           ok = false;
           break;
         }
@@ -532,7 +534,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       l += (sq[0] + sq[1]) + (sq[2] + sq[3]);
       // P buffer sb was last read by P.V of step j-2
       if (j >= 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.pv_done[sb], ((j - 2) / 2) & 1, abort))) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_abortable(&sh.k_empty[(j - 2) % kStages], ((j - 2) / kStages) & 1, abort))) {
           ok = false;
           break;
         }
@@ -551,7 +554,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     const float l_o = fin[((set ^ 1) * 2 + 0) * kTileRows + r], m_o = fin[((set ^ 1) * 2 + 1) * kTileRows + r];
     const float m_fin = fmaxf(m_ref, m_o);
     const float lrow = (l > 0.f ? l * fast_exp2(m_ref - m_fin) : 0.f) + (l_o > 0.f ? l_o * fast_exp2(m_o - m_fin) : 0.f);
-    if (ok && !mbar_wait_abortable(&sh.pv_done[(ntiles - 1) % 2], ((ntiles - 1) / 2) & 1, abort)) ok = false;
+    if (ok && !mbar_wait_abortable(&sh.k_empty[(ntiles - 1) % kStages], ((ntiles - 1) / kStages) & 1, abort))
+      ok = false;
     tc_fence_after();
     if (__all_sync(0xffffffffu, ok)) {
       const int64_t prow = (static_cast<int64_t>(b) * p.max_splits + split) * (p.row_tiles * kTileRows) + grow;
