@@ -142,6 +142,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
+  // the merge kernel may be scheduled once every CTA of this grid has started:
+  // it then occupies only SMs freed by finished CTAs and waits for this grid
+  // to complete before it reads the partials
+  grid_dep_launch();
   const int split = blockIdx.x >> 1;
   const int row_tile = blockIdx.y;
   const int b = blockIdx.z;

@@ -290,6 +290,14 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream still runs,
+// once every CTA of that kernel has executed launch_dependents (or exited);
+// wait blocks until the previous kernel has completed and its writes are
+// visible (a no-op without such a predecessor).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 2^x with the SFU instruction (ex2.approx.ftz.f32; 2^-inf = +0).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

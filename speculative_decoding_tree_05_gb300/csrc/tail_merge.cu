@@ -18,6 +18,8 @@
 //   tail:  s_u = scale * q.k_u for the visible u, online softmax, o_t = sum p_u v_u
 //   merge: lse = log2-sum-exp over {tail, prefix splits}, out = weighted sum of
 //          the normalised partial outputs; lse is reported in natural log.
+// Launched as a programmatic dependent of the prefix pass: everything before
+// the merge step runs while the prefix pass finishes.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include "kernels.cuh"
@@ -92,13 +94,6 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
   const int64_t pstride = static_cast<int64_t>(p.row_tiles) * kTileRows;
   const int64_t pbase = static_cast<int64_t>(b) * p.max_splits * pstride + r;
 
-  // prefix split lse values, one per lane (up to 32 at a time), issued before the tail math
-  float lse_l[2];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int s = lane + 32 * k;
-    lse_l[k] = s < splits ? __ldg(p.lse_part + pbase + s * pstride) * kLog2e : -CUDART_INF_F;
-  }
   // q: lane holds dims {64 i + 2 lane, +1}, i = 0..8
   uint32_t qv[9];
   const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + grow * kDqk);
@@ -138,12 +133,24 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
     }
   }
 
+  // Everything above is independent of the prefix pass, which may still be
+  // running (programmatic dependent launch); the partials are read only now,
+  // through L2 (ld.global.cg), since another SM wrote them.
+  grid_dep_wait();
+  // prefix split lse values, one per lane (up to 64 here, the rest in the loops)
+  float lse_l[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int s = lane + 32 * k;
+    lse_l[k] = s < splits ? __ldcg(p.lse_part + pbase + s * pstride) * kLog2e : -CUDART_INF_F;
+  }
+
   // merge: weights 2^(lse_part - max) over the tail and every split
   const float lse2_t = (l > 0.f) ? m + log2f(l) : -CUDART_INF_F;
   float mx = fmaxf(lse_l[0], lse_l[1]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  for (int s = 64; s < splits; ++s) mx = fmaxf(mx, __ldg(p.lse_part + pbase + s * pstride) * kLog2e);
+  for (int s = 64; s < splits; ++s) mx = fmaxf(mx, __ldcg(p.lse_part + pbase + s * pstride) * kLog2e);
   mx = fmaxf(mx, lse2_t);
 
   float acc[16];
@@ -166,13 +173,13 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
       for (int u = 0; u < 4; ++u) {
         const float4* op = reinterpret_cast<const float4*>(p.o_part + (pbase + (s + u) * pstride) * kDv);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) x[u][j] = __ldg(op + lane + 32 * j);
+        for (int j = 0; j < 4; ++j) x[u][j] = __ldcg(op + lane + 32 * j);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int su = s + u;
         float ws = __shfl_sync(0xffffffffu, (su & 32) ? wl1 : wl0, su & 31);
-        if (su >= 64) ws = fast_exp2(__ldg(p.lse_part + pbase + su * pstride) * kLog2e - mx);
+        if (su >= 64) ws = fast_exp2(__ldcg(p.lse_part + pbase + su * pstride) * kLog2e - mx);
         wsum += ws;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -186,11 +193,11 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
     for (; s < splits; ++s) {
       const float4* op = reinterpret_cast<const float4*>(p.o_part + (pbase + s * pstride) * kDv);
       float ws = __shfl_sync(0xffffffffu, (s & 32) ? wl1 : wl0, s & 31);
-      if (s >= 64) ws = fast_exp2(__ldg(p.lse_part + pbase + s * pstride) * kLog2e - mx);
+      if (s >= 64) ws = fast_exp2(__ldcg(p.lse_part + pbase + s * pstride) * kLog2e - mx);
       wsum += ws;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float4 x = __ldg(op + lane + 32 * j);
+        const float4 x = __ldcg(op + lane + 32 * j);
         acc[4 * j + 0] = fmaf(ws, x.x, acc[4 * j + 0]);
         acc[4 * j + 1] = fmaf(ws, x.y, acc[4 * j + 1]);
         acc[4 * j + 2] = fmaf(ws, x.z, acc[4 * j + 2]);
@@ -214,9 +221,18 @@ cudaError_t configure_tail_merge() {
 
 cudaError_t launch_tail_merge(const TailParams& p, int batch, cudaStream_t stream) {
   const int smem = p.nodes * kRowBytes;
-  dim3 grid(p.nodes, (p.heads + p.heads_per_cta - 1) / p.heads_per_cta, batch);
-  tail_merge_kernel<<<grid, kTailThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the prologue and tree tail overlap the end of the prefix pass
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(p.nodes, (p.heads + p.heads_per_cta - 1) / p.heads_per_cta, batch);
+  cfg.blockDim = dim3(kTailThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tail_merge_kernel, p);
 }
 
 }  // namespace ddt
