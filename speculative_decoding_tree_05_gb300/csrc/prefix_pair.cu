@@ -40,13 +40,12 @@
 // the split merge, off by the same rounding).
 //
 // Per CTA (384 threads):
-//   warp 0      TMEM allocation; lane 0 issues every tcgen05.mma.  A
-//               tcgen05.mma costs about 45 issue cycles whatever its shape, so
-//               each MMA is at least M=128 x N=64 (scores) or N=256 (P.V).
-//               The issuer polls its barriers and issues whichever is ready:
-//               S of the next step (its stage loaded and the one S buffer
-//               read out by the softmax) or P.V of the oldest step whose P
-//               is written, so scores run ahead of the softmax and exchange.
+//   warp 0      TMEM allocation; lane 0 issues the score MMAs S(t) once the
+//               stage is loaded and S(t-1) has been read out of the S buffer.
+//               A tcgen05.mma costs about 45 issue cycles whatever its shape,
+//               so each MMA is at least M=128 x N=64 (scores) or N=256 (P.V);
+//               the pipe takes the next MMA only about as fast as it runs one,
+//               so P.V is issued by the softmax set that wrote its P.
 //   warps 1-3   producers: load the CTA's dims of 64 slot rows per step into a
 //               5-stage ring, the step's slot indices fetched one step ahead.
 //               A step whose 64 slots are consecutive (a compacted pool) is 5
@@ -123,6 +122,8 @@ struct Shared {
   uint64_t x_free[kXBufs];    // peer's softmax warps -> sender: step t read from the peer's buffer t % 2
   uint64_t m_ready[2];        // softmax set -> other set: running max after step t in hand[t % 2]
   uint64_t q_ready;           // softmax -> MMA: Q_r staged
+  uint64_t mma_drain;         // the three MMA-issuing threads: every MMA issued has completed
+  volatile int pv_next;       // the step whose P.V is issued next (P.V goes in step order)
   uint32_t tmem_base;
   int abort;
 };
@@ -181,6 +182,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       mbar_init(&sh.x_free[i], 4);  // the 4 warps of the peer's set
     }
     mbar_init(&sh.q_ready, 256);
+    mbar_init(&sh.mma_drain, 3);  // one commit from each MMA-issuing thread
+    sh.pv_next = 0;
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -196,63 +199,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
   int issued = 0;  // producers: steps this warp has issued loads for
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ S issuer
+    // The tensor pipe takes the next MMA only about as fast as it runs one, so a
+    // thread that also issued P.V could not react to the read-out of S while
+    // inside a P.V group: this thread issues only S, sleeping on the barrier it
+    // needs; each softmax set issues the P.V of its own steps.
     if (lane == 0) {
       if (!mbar_wait_abortable(&sh.q_ready, 0, abort)) ok = false;
       fence_proxy_async_smem();  // Q rope dims were stored to shared memory by the softmax threads
       tc_fence_after();
       // operand descriptors of stage 0, built once; a stage or k-step is an offset
-      // (the issuing thread is serial and each MMA issue waits for the pipe, so
-      // rebuilding descriptors between MMAs would stretch every MMA)
       const uint64_t d_lat = smem_desc(stage0, 16, 1024, kSwizzle128B);             // K of S: K-major
       const uint64_t d_rope = smem_desc(stage0 + 4 * kLatBlock, 16, 512, kSwizzle64B);
       const uint64_t d_qrope = smem_desc(qrope_s, 16, 512, kSwizzle64B);
-      const uint64_t d_v = smem_desc(stage0, kLatBlock, 1024, kSwizzle128B);         // V of P.V: MN-major
-      int ns = 0, np = 0;        // next step whose S / P.V is to be issued
-      uint32_t idle = 0;
-      while (ok && np < ntiles) {
-        bool progressed = false;
-        // S(ns): stage loaded, and S(ns-1) read out of the S buffer
-        if (ns < ntiles && mbar_test_wait(&sh.k_full[ns % kStages], (ns / kStages) & 1) &&
-            (ns == 0 || mbar_test_wait(&sh.s_free[(ns - 1) % 2], ((ns - 1) / 2) & 1))) {
-          // the stage may have been written by cp.async (generic proxy): order it
-          // before the tensor core's async-proxy reads
-          fence_proxy_async_smem();
-          tc_fence_after();
-          const uint32_t so = (ns % kStages) * kStageBytes;
-          const uint64_t dl = desc_advance(d_lat, so), dr = desc_advance(d_rope, so);
-#pragma unroll
-          for (int ks = 0; ks < 16; ++ks)
-            mma_ts(tmem + kColS, tmem + kColQ + ks * 8, desc_advance(dl, (ks >> 2) * kLatBlock + (ks & 3) * 32), kIdescS,
-                   ks > 0 ? 1u : 0u);
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks)
-            mma_ss(tmem + kColS, desc_advance(d_qrope, ks * 32), desc_advance(dr, ks * 32), kIdescS, 1u);
-          mma_commit(&sh.s_full[ns % 2]);
-          ++ns;
-          progressed = true;
-        }
-        // P.V(np): P written (and O rescaled) by its softmax set
-        if (np < ns && mbar_test_wait(&sh.p_ready[np % 2], (np / 2) & 1)) {
-          tc_fence_after();
-          const uint64_t dv = desc_advance(d_v, (np % kStages) * kStageBytes);
-          const uint32_t pb = tmem + kColP + (np % 2) * (kNk / 2);
-#pragma unroll
-          for (int ks = 0; ks < kNk / 16; ++ks)
-            mma_ts(tmem + kColO, pb + ks * 8, desc_advance(dv, ks * 16 * 128), kIdescPV, (np > 0 || ks > 0) ? 1u : 0u);
-          // one commit per MMA group: k_empty[stage] also tells the softmax that
-          // P.V(np) is done (a second commit straight after a first cannot be
-          // relied on to wait for the same MMAs)
-          mma_commit(&sh.k_empty[np % kStages]);
-          ++np;
-          progressed = true;
-        }
-        if (progressed) {
-          idle = 0;
-        } else if (++idle > (1u << 26) || ((idle & 255) == 255 && *abort)) {
+      for (int ns = 0; ok && ns < ntiles; ++ns) {
+        // stage loaded, and S(ns-1) read out of the S buffer
+        if (!mbar_wait_abortable(&sh.k_full[ns % kStages], (ns / kStages) & 1, abort) ||
+            (ns > 0 && !mbar_wait_abortable(&sh.s_free[(ns - 1) % 2], ((ns - 1) / 2) & 1, abort))) {
           ok = false;
+          break;
         }
+        // the stage may have been written by cp.async (generic proxy): order it
+        // before the tensor core's async-proxy reads
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const uint32_t so = (ns % kStages) * kStageBytes;
+        const uint64_t dl = desc_advance(d_lat, so), dr = desc_advance(d_rope, so);
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks)
+          mma_ts(tmem + kColS, tmem + kColQ + ks * 8, desc_advance(dl, (ks >> 2) * kLatBlock + (ks & 3) * 32), kIdescS,
+                 ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          mma_ss(tmem + kColS, desc_advance(d_qrope, ks * 32), desc_advance(dr, ks * 32), kIdescS, 1u);
+        mma_commit(&sh.s_full[ns % 2]);
       }
+      // nothing of this thread's may still be running when TMEM is released (also after a timeout)
+      mma_commit(&sh.mma_drain);
+      mbar_wait(&sh.mma_drain, 0, 1u << 20);
     }
     __syncwarp();
   } else if (warp < 4) {
@@ -395,7 +379,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       xfree_remote[i] = mapa_shared(smem_u32(&sh.x_free[i]), peer);
     }
     const int32_t* slots = p.slot_idx + static_cast<int64_t>(b) * p.slot_stride;
-    const bool lead = (warp & 3) == 0 && lane == 0;    // row 0 of this set
+    const bool lead = (warp & 3) == 0 && lane == 0;    // row 0 of this set; issues the set's P.V
+    const uint64_t d_v = smem_desc(stage0, kLatBlock, 1024, kSwizzle128B);  // V of P.V: MN-major
     float m_used = -CUDART_INF_F;                      // running max after the last step seen
     float m_ref = -CUDART_INF_F, l = 0.f;              // this set's row sum, relative to m_ref
     auto fetch_slot = [&](int j, int e) -> int {
@@ -548,6 +533,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       tmem_st32(tmem + lane_off + kColP + sb * (kNk / 2), pk);
       tc_fence_before();
       mbar_arrive(&sh.p_ready[sb]);
+      // P.V(j), issued by the set's first thread once every row of P(j) is in
+      // TMEM and, to keep P.V in step order (the lazy rescale of O relies on
+      // it), once the other set has issued P.V(j-1).  One commit per group:
+      // k_empty[stage] also tells everyone that P.V(j) is done.
+      bool pv_ok = true;
+      if (lead) {
+        pv_ok = mbar_wait_abortable(&sh.p_ready[sb], (j / 2) & 1, abort);
+        for (uint32_t spin = 0; pv_ok && sh.pv_next != j; ++spin)
+          if (spin > (1u << 24) || ((spin & 255) == 255 && *abort)) pv_ok = false;
+        if (pv_ok) {
+          tc_fence_after();
+          const uint64_t dv = desc_advance(d_v, (j % kStages) * kStageBytes);
+          const uint32_t pb = tmem + kColP + sb * (kNk / 2);
+#pragma unroll
+          for (int ks = 0; ks < kNk / 16; ++ks)
+            mma_ts(tmem + kColO, pb + ks * 8, desc_advance(dv, ks * 16 * 128), kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(&sh.k_empty[j % kStages]);
+          sh.pv_next = j + 1;
+        }
+      }
+      if (!__all_sync(0xffffffffu, pv_ok)) {
+        ok = false;
+        break;
+      }
     }
 
     // epilogue: combine both sets' row sums, wait for the last P.V, then
@@ -580,6 +589,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     }
   }
 
+  if (warp >= 4 && (warp & 3) == 0 && lane == 0) {
+    // the P.V MMAs this thread issued: all complete before TMEM is released (also after a timeout)
+    mma_commit(&sh.mma_drain);
+    mbar_wait(&sh.mma_drain, 0, 1u << 20);
+  }
   if (!ok) {
     *abort = 1;
     atomicOr(p.status, kStatusTimeout);
