@@ -573,16 +573,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     if (__all_sync(0xffffffffu, ok)) {
       const int64_t prow = (static_cast<int64_t>(b) * p.max_splits + split) * (p.row_tiles * kTileRows) + grow;
       const float inv_l = lrow > 0.f ? 1.f / lrow : 0.f;
+      // A thread holds one row, so storing straight from registers would touch
+      // 32 rows (32 lines) per store instruction.  Each warp instead stages a
+      // 32-row x 32-column chunk in the stage ring (idle now: every P.V is done)
+      // and stores it back as 4 row segments of 128 bytes per instruction.
+      uint8_t* stage_w = smem + (warp - 4) * (kTileRows / 4 * 32 * 4);  // 4 KB per softmax warp
+      const int row0 = row_tile * kTileRows + (warp & 3) * 32;          // first row of this warp
+      const int64_t prow0 = prow - lane;
 #pragma unroll 1
       for (int c = 0; c < 128; c += 32) {
         float o[32];
         tmem_ld32(tmem + lane_off + kColO + 128 * set + c, o);
-        if (row_valid) {
-          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * kDv + 256 * rank + 128 * set + c);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(o[4 * k] * inv_l, o[4 * k + 1] * inv_l, o[4 * k + 2] * inv_l, o[4 * k + 3] * inv_l);
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<float4*>(stage_w + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+              make_float4(o[4 * k] * inv_l, o[4 * k + 1] * inv_l, o[4 * k + 2] * inv_l, o[4 * k + 3] * inv_l);
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int rr = 4 * it + (lane >> 3), u = lane & 7;  // row of the warp, 16-byte unit of the chunk
+          const float4 v = *reinterpret_cast<const float4*>(stage_w + rr * 128 + ((u ^ (rr & 7)) << 4));
+          if (row0 + rr < p.rows)
+            *reinterpret_cast<float4*>(p.o_part + (prow0 + rr) * kDv + 256 * rank + 128 * set + c + 4 * u) = v;
         }
+        __syncwarp();
       }
       if (rank == 0 && set == 0 && row_valid)
         p.lse_part[prow] = lrow > 0.f ? (m_fin + log2f(lrow)) * kLn2 : -CUDART_INF_F;
