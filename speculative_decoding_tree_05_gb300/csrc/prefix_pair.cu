@@ -90,6 +90,7 @@ constexpr int kLatBlock = kNk * 128;                     // 8192
 constexpr int kRopeBlock = kNk * 64;                     // 4096
 constexpr int kStageBytes = 4 * kLatBlock + kRopeBlock;  // 36864
 constexpr int kProducers = 96;
+constexpr int kSlotLookahead = 4;                        // producers fetch slot indices this many steps ahead
 constexpr int kGatherBlocks = 3;                         // latent blocks fetched by gather4 on scattered steps
 constexpr int kXBufs = 2;                                // exchange buffers (step t uses t % 2)
 constexpr int kXBytes = kTileRows * kNk * 2;             // 16384: int16 mantissas of one step
@@ -191,8 +192,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     tmem_alloc(&sh.tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  // Global reads that need no set-up are issued before the CTA's barrier, so
+  // their latency overlaps it: the producers' slot indices of the first steps
+  // (lane l holds the slots of keys l and l+32 of a step; -1 past the split
+  // end) and the softmax threads' query row.
+  const int32_t* slots = p.slot_idx + static_cast<int64_t>(b) * p.slot_stride;
+  auto fetch = [&](int j, int e) -> int {
+    const int key = kbegin + j * kNk + lane + 32 * e;
+    return key < kend ? __ldg(slots + key) : -1;
+  };
+  const bool producer = warp >= 1 && warp < 4;
+  int pf[2 * kSlotLookahead];
+#pragma unroll
+  for (int i = 0; i < 2 * kSlotLookahead; ++i) pf[i] = producer ? fetch(i >> 1, i & 1) : -1;
+  const int qrow = (warp & 3) * 32 + lane;
+  const bool q_valid = warp >= 4 && row_tile * kTileRows + qrow < p.rows;
+  const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(b) * p.rows + row_tile * kTileRows + qrow) * kDqk);
+  uint4 qv[16 + 4];
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    qv[c] = q_valid ? __ldg(qsrc + 32 * rank + 16 * ((warp - 4) >> 2) + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) qv[16 + c] = q_valid && warp < 8 ? __ldg(qsrc + 64 + 4 * rank + c) : make_uint4(0, 0, 0, 0);
   tc_fence_before();
-  cluster_sync();  // both CTAs' barriers exist before any remote arrive
+  __syncthreads();  // this CTA's barriers initialised and its TMEM allocated
+  // The peer addresses this CTA's barriers only after its own cluster_wait,
+  // which follows this arrive: threads that touch the peer wait before their
+  // first remote access, the others before the final cluster barrier.
+  cluster_arrive();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
   bool ok = true;
@@ -239,17 +266,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       mbar_wait(&sh.mma_drain, 0, 1u << 20);
     }
     __syncwarp();
+    cluster_wait();
   } else if (warp < 4) {
     // ------------------------------------------------------------------ producers
     const int ptid = tid - 32;
-    const int32_t* slots = p.slot_idx + static_cast<int64_t>(b) * p.slot_stride;
     const uint16_t* kv = p.kv;
     const int rk = static_cast<int>(rank);
-    // lane l holds the slots of keys l and l+32 of a step (fetched one step ahead); -1 past the split end
-    auto fetch = [&](int j, int e) -> int {
-      const int key = kbegin + j * kNk + lane + 32 * e;
-      return key < kend ? __ldg(slots + key) : -1;
-    };
     auto in_pool = [&](int s_) { return s_ >= 0 && static_cast<int64_t>(s_) < p.pool_slots; };
     // 16-byte chunk c of the CTA's 36 per row -> (source column, smem offset in the stage):
     // c < 32 latent block c/8 (128-byte swizzle), c >= 32 the rope block (64-byte swizzle)
@@ -258,10 +280,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
                     : 4 * kLatBlock + n * 64 + (((c - 32) ^ ((n >> 1) & 3)) << 4);
     };
     auto chunk_col = [&](int c) -> int { return c < 32 ? 256 * rk + 8 * c : 512 + 32 * rk + 8 * (c - 32); };
-    int cur0 = fetch(0, 0), cur1 = fetch(0, 1);
+    // slot indices are fetched kSlotLookahead steps ahead: under a gather-heavy
+    // load their latency exceeds a step
     for (int j = 0; j < ntiles; ++j) {
-      const int nxt0 = (j + 1 < ntiles) ? fetch(j + 1, 0) : -1;
-      const int nxt1 = (j + 1 < ntiles) ? fetch(j + 1, 1) : -1;
+      const int cur0 = pf[0], cur1 = pf[1];
+#pragma unroll
+      for (int i = 0; i + 2 < 2 * kSlotLookahead; ++i) pf[i] = pf[i + 2];
+      pf[2 * kSlotLookahead - 2] = fetch(j + kSlotLookahead, 0);
+      pf[2 * kSlotLookahead - 1] = fetch(j + kSlotLookahead, 1);
       const int st = j % kStages;
       // warp-uniform wait: the lane shuffles below need every lane
       const bool waited = j < kStages || mbar_wait_abortable(&sh.k_empty[st], ((j / kStages) - 1) & 1, abort);
@@ -329,10 +355,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       }
       cp_async_arrive_noinc(&sh.k_full[st]);
       issued = j + 1;
-      cur0 = nxt0;
-      cur1 = nxt1;
     }
     cp_async_wait<0>();
+    cluster_wait();
   } else {
     // ------------------------------------------------------------------ softmax sets + epilogue
     const int set = (warp - 4) >> 2;                   // 0: even steps, 1: odd steps
@@ -343,31 +368,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     float* hand = reinterpret_cast<float*>(smem + kOffHand);   // [2][128]
     float* fin = reinterpret_cast<float*>(smem + kOffFin);     // [2 sets][2][128]
 
-    // Q_r: latent dims [256 rank + 128 set, +128) -> TMEM, rope dims [512 + 32 rank, +32) -> smem
+    // Q_r (read into registers before the CTA barrier): latent dims
+    // [256 rank + 128 set, +128) -> TMEM, rope dims [512 + 32 rank, +32) -> smem
     {
-      const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(b) * p.rows + grow) * kDqk);
-      const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll 1
+#pragma unroll
       for (int c0 = 0; c0 < 16; c0 += 8) {
         uint32_t v[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 x = row_valid ? __ldg(qsrc + 32 * rank + 16 * set + c0 + c) : zero;
-          v[4 * c] = x.x, v[4 * c + 1] = x.y, v[4 * c + 2] = x.z, v[4 * c + 3] = x.w;
-        }
+        for (int c = 0; c < 8; ++c)
+          v[4 * c] = qv[c0 + c].x, v[4 * c + 1] = qv[c0 + c].y, v[4 * c + 2] = qv[c0 + c].z, v[4 * c + 3] = qv[c0 + c].w;
         tmem_st32(tmem + lane_off + kColQ + 64 * set + c0 * 4, v);
       }
       if (set == 0) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 x = row_valid ? __ldg(qsrc + 64 + 4 * rank + c) : zero;
-          *reinterpret_cast<uint4*>(qrope + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = x;
-        }
+        for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(qrope + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = qv[16 + c];
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sh.q_ready);
     }
+    cluster_wait();  // the peer's barriers exist before the first exchange
 
     const uint32_t peer = rank ^ 1u;
     const uint32_t x_remote = mapa_shared(stage0 + kOffX, peer);
@@ -378,7 +398,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       xbar_remote[i] = mapa_shared(smem_u32(&sh.x_full[i]), peer);
       xfree_remote[i] = mapa_shared(smem_u32(&sh.x_free[i]), peer);
     }
-    const int32_t* slots = p.slot_idx + static_cast<int64_t>(b) * p.slot_stride;
     const bool lead = (warp & 3) == 0 && lane == 0;    // row 0 of this set; issues the set's P.V
     const uint64_t d_v = smem_desc(stage0, kLatBlock, 1024, kSwizzle128B);  // V of P.V: MN-major
     float m_used = -CUDART_INF_F;                      // running max after the last step seen
