@@ -429,11 +429,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       // encode own partial (block floating point) and send it; the own partial stays unrounded
       float am[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains: a 64-long max chain is latency-bound
 #pragma unroll
-      for (int k = 0; k < 64; ++k) am[k & 3] = fmaxf(am[k & 3], fabsf(x[k]));
+      for (int k = 0; k < 64; k += 2) am[(k >> 1) & 3] = fmax3(am[(k >> 1) & 3], fabsf(x[k]), fabsf(x[k + 1]));
       const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
       const float sl2 = p.scale_log2;
       const int e = block_exponent(amax * sl2);
       const float enc = sl2 * pow2i(14 - e);
+      const uint64_t enc2 = f32x2(enc, enc), magic2 = f32x2(kMagic, kMagic);
       // the peer must have read step j-2 out of the buffer before it is overwritten
       if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_free[xb_i], ((j - 2) / 2) & 1, abort, true))) {
         ok = false;
@@ -448,7 +449,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int k = 8 * c + 2 * q;
-            const float t0 = fmaf(x[k], enc, kMagic), t1 = fmaf(x[k + 1], enc, kMagic);
+            float t0, t1;
+            f32x2_split(fma_x2(f32x2(x[k], x[k + 1]), enc2, magic2), t0, t1);
             w[q] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
           }
           st_async_v4(xr + c * (kTileRows * 16), make_uint4(w[0], w[1], w[2], w[3]), br);
@@ -470,6 +472,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         const uint8_t* xbp = smem + kOffX + xb_i * kXBytes + r * 16;
         const int pe = *reinterpret_cast<const int*>(smem + kOffE + xb_i * kEBytes + r * 4);
         const float pdec = pow2i(pe - 14), pm = -kMagic * pdec;
+        const uint64_t pdec2 = f32x2(pdec, pdec), pm2 = f32x2(pm, pm), sl22 = f32x2(sl2, sl2);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint4 v = *reinterpret_cast<const uint4*>(xbp + c * (kTileRows * 16));
@@ -477,10 +480,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int k = 8 * c + 2 * q;
-            const float a = fmaf(__uint_as_float(__byte_perm(w[q], kMagicHi, 0x7610)), pdec, pm);
-            const float bb = fmaf(__uint_as_float(__byte_perm(w[q], kMagicHi, 0x7632)), pdec, pm);
-            x[k] = fmaf(x[k], sl2, a);
-            x[k + 1] = fmaf(x[k + 1], sl2, bb);
+            const uint64_t peer = fma_x2(f32x2(__uint_as_float(__byte_perm(w[q], kMagicHi, 0x7610)),
+                                               __uint_as_float(__byte_perm(w[q], kMagicHi, 0x7632))),
+                                         pdec2, pm2);
+            f32x2_split(fma_x2(f32x2(x[k], x[k + 1]), sl22, peer), x[k], x[k + 1]);
           }
         }
         __syncwarp();
@@ -492,7 +495,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         }
         float mq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-        for (int k = 0; k < 64; ++k) mq[k & 3] = fmaxf(mq[k & 3], x[k]);
+        for (int k = 0; k < 64; k += 2) mq[(k >> 1) & 3] = fmax3(mq[(k >> 1) & 3], x[k], x[k + 1]);
         mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       }
       // running max after step j-1 comes from the other set
@@ -531,15 +534,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         m_ref = m_used;
       }
       const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
-      float sq[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t sq[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+      const uint64_t msub2 = f32x2(msub, msub);
       uint32_t pk[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        const float p0 = fast_exp2(x[2 * k] - msub), p1 = fast_exp2(x[2 * k + 1] - msub);
-        sq[k & 3] += p0 + p1;
+        float d0, d1;
+        f32x2_split(sub_x2(f32x2(x[2 * k], x[2 * k + 1]), msub2), d0, d1);
+        const float p0 = fast_exp2(d0), p1 = fast_exp2(d1);
+        sq[k & 1] = add_x2(sq[k & 1], f32x2(p0, p1));
         pk[k] = pack_bf16x2(p0, p1);
       }
-      l += (sq[0] + sq[1]) + (sq[2] + sq[3]);
+      float s0, s1, s2, s3;
+      f32x2_split(sq[0], s0, s1);
+      f32x2_split(sq[1], s2, s3);
+      l += (s0 + s1) + (s2 + s3);
       // P buffer sb was last read by P.V of step j-2
       if (j >= 2) {
         if (!__all_sync(0xffffffffu,
