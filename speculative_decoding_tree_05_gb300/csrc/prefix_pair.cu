@@ -92,17 +92,21 @@ constexpr int kStageBytes = 4 * kLatBlock + kRopeBlock;  // 36864
 constexpr int kProducers = 96;
 constexpr int kSlotLookahead = 4;                        // producers fetch slot indices this many steps ahead
 constexpr int kGatherBlocks = 3;                         // latent blocks fetched by gather4 on scattered steps
-constexpr int kXBufs = 2;                                // exchange buffers (step t uses t % 2)
+constexpr int kXSets = 2;                                // exchange barrier pairs (step t uses t % 2)
 constexpr int kXBytes = kTileRows * kNk * 2;             // 16384: int16 mantissas of one step
 constexpr int kEBytes = kTileRows * 4;                   // 512: one exponent per row
 constexpr int kQRopeBytes = kTileRows * 64;              // 8192: Q_r rope dims, 64-byte swizzle
-constexpr int kOffX = kStages * kStageBytes;
-constexpr int kOffE = kOffX + kXBufs * kXBytes;
-constexpr int kOffQRope = kOffE + kXBufs * kEBytes;
+constexpr int kQLatSmemBytes = kTileRows * 128;          // 16384: Q_r latent dims 192..255, 128-byte swizzle
+constexpr int kOffQLat = kStages * kStageBytes;          // 1024-byte aligned (128-byte swizzle atoms)
+constexpr int kOffX = kOffQLat + kQLatSmemBytes;         // one exchange buffer: a step is read out before the next is sent
+constexpr int kOffE = kOffX + kXBytes;
+constexpr int kOffQRope = kOffE + kEBytes;               // 512-byte aligned (64-byte swizzle atoms)
+static_assert(kOffQLat % 1024 == 0 && kOffQRope % 512 == 0, "swizzled operands need aligned bases");
 constexpr int kOffHand = kOffQRope + kQRopeBytes;        // [2][128] running max handed between sets
 constexpr int kOffFin = kOffHand + 2 * kTileRows * 4;    // [2 sets][2 (l, m)][128] final row state
 constexpr int kSmem = kOffFin + 2 * 2 * kTileRows * 4 + 1024;
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 384, kTmemCols = 512;
+constexpr uint32_t kColO = 0, kColS = 256, kColP = 384, kColQ = 416, kTmemCols = 512;
+constexpr int kQTmemKSteps = 12;                         // Q_r latent dims 0..191 from TMEM, 192..255 from smem
 constexpr uint32_t kIdescS = idesc_bf16_f32(kTileRows, kNk, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileRows, 256, false, true);
 constexpr float kRescaleThreshold = 8.f;                 // log2 units
@@ -118,9 +122,9 @@ struct Shared {
                               // (phase t / kStages of k_empty[t % kStages])
   uint64_t s_full[2];         // MMA -> softmax set t%2: partial scores of step t in the S buffer
   uint64_t s_free[2];         // softmax set t%2 -> MMA: S of step t loaded into registers
-  uint64_t p_ready[2];        // softmax set -> MMA: P of step t in P buffer t % 2, O rescaled
-  uint64_t x_full[kXBufs];    // peer -> softmax: peer's partial scores of step t in buffer t % 2
-  uint64_t x_free[kXBufs];    // peer's softmax warps -> sender: step t read from the peer's buffer t % 2
+  uint64_t p_ready[2];        // softmax set t%2 -> its P.V issuer: P of step t in the P buffer, O rescaled
+  uint64_t x_full[kXSets];    // peer -> softmax set t%2: peer's partial scores of step t in the exchange buffer
+  uint64_t x_free[kXSets];    // peer's set t%2 -> sender: step t read out of the peer's exchange buffer
   uint64_t m_ready[2];        // softmax set -> other set: running max after step t in hand[t % 2]
   uint64_t q_ready;           // softmax -> MMA: Q_r staged
   uint64_t mma_drain;         // the three MMA-issuing threads: every MMA issued has completed
@@ -178,7 +182,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       mbar_init(&sh.p_ready[i], 128);
       mbar_init(&sh.m_ready[i], 128);
     }
-    for (int i = 0; i < kXBufs; ++i) {
+    for (int i = 0; i < kXSets; ++i) {
       mbar_init(&sh.x_full[i], 1);
       mbar_init(&sh.x_free[i], 4);  // the 4 warps of the peer's set
     }
@@ -239,10 +243,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       const uint64_t d_lat = smem_desc(stage0, 16, 1024, kSwizzle128B);             // K of S: K-major
       const uint64_t d_rope = smem_desc(stage0 + 4 * kLatBlock, 16, 512, kSwizzle64B);
       const uint64_t d_qrope = smem_desc(qrope_s, 16, 512, kSwizzle64B);
+      const uint64_t d_qlat = smem_desc(stage0 + kOffQLat, 16, 1024, kSwizzle128B);
       for (int ns = 0; ok && ns < ntiles; ++ns) {
-        // stage loaded, and S(ns-1) read out of the S buffer
+        // stage loaded, and S(ns-2) read out of S buffer ns % 2
         if (!mbar_wait_abortable(&sh.k_full[ns % kStages], (ns / kStages) & 1, abort) ||
-            (ns > 0 && !mbar_wait_abortable(&sh.s_free[(ns - 1) % 2], ((ns - 1) / 2) & 1, abort))) {
+            (ns > 1 && !mbar_wait_abortable(&sh.s_free[ns % 2], ((ns - 2) / 2) & 1, abort))) {
           ok = false;
           break;
         }
@@ -252,13 +257,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         tc_fence_after();
         const uint32_t so = (ns % kStages) * kStageBytes;
         const uint64_t dl = desc_advance(d_lat, so), dr = desc_advance(d_rope, so);
+        const uint32_t sd = tmem + kColS + (ns % 2) * kNk;
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks)
-          mma_ts(tmem + kColS, tmem + kColQ + ks * 8, desc_advance(dl, (ks >> 2) * kLatBlock + (ks & 3) * 32), kIdescS,
+        for (int ks = 0; ks < kQTmemKSteps; ++ks)
+          mma_ts(sd, tmem + kColQ + ks * 8, desc_advance(dl, (ks >> 2) * kLatBlock + (ks & 3) * 32), kIdescS,
                  ks > 0 ? 1u : 0u);
 #pragma unroll
+        for (int ks = kQTmemKSteps; ks < 16; ++ks)
+          mma_ss(sd, desc_advance(d_qlat, (ks - kQTmemKSteps) * 32),
+                 desc_advance(dl, (ks >> 2) * kLatBlock + (ks & 3) * 32), kIdescS, 1u);
+#pragma unroll
         for (int ks = 0; ks < 2; ++ks)
-          mma_ss(tmem + kColS, desc_advance(d_qrope, ks * 32), desc_advance(dr, ks * 32), kIdescS, 1u);
+          mma_ss(sd, desc_advance(d_qrope, ks * 32), desc_advance(dr, ks * 32), kIdescS, 1u);
         mma_commit(&sh.s_full[ns % 2]);
       }
       // nothing of this thread's may still be running when TMEM is released (also after a timeout)
@@ -368,16 +378,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     float* hand = reinterpret_cast<float*>(smem + kOffHand);   // [2][128]
     float* fin = reinterpret_cast<float*>(smem + kOffFin);     // [2 sets][2][128]
 
-    // Q_r (read into registers before the CTA barrier): latent dims
-    // [256 rank + 128 set, +128) -> TMEM, rope dims [512 + 32 rank, +32) -> smem
+    // Q_r (read into registers before the CTA barrier): set s holds latent dims
+    // [256 rank + 128 s, +128); dims 0..191 of the CTA's 256 go to TMEM, dims
+    // 192..255 (the second half of set 1's) to shared memory, 128-byte swizzle;
+    // rope dims [512 + 32 rank, +32) -> shared memory, 64-byte swizzle
     {
 #pragma unroll
       for (int c0 = 0; c0 < 16; c0 += 8) {
-        uint32_t v[32];
+        if (set == 1 && c0 == 8) {
+          uint8_t* ql = smem + kOffQLat + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          v[4 * c] = qv[c0 + c].x, v[4 * c + 1] = qv[c0 + c].y, v[4 * c + 2] = qv[c0 + c].z, v[4 * c + 3] = qv[c0 + c].w;
-        tmem_st32(tmem + lane_off + kColQ + 64 * set + c0 * 4, v);
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(ql + ((c ^ (r & 7)) << 4)) = qv[8 + c];
+        } else {
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            v[4 * c] = qv[c0 + c].x, v[4 * c + 1] = qv[c0 + c].y, v[4 * c + 2] = qv[c0 + c].z, v[4 * c + 3] = qv[c0 + c].w;
+          tmem_st32(tmem + lane_off + kColQ + 64 * set + c0 * 4, v);
+        }
       }
       if (set == 0) {
 #pragma unroll
@@ -392,9 +410,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     const uint32_t peer = rank ^ 1u;
     const uint32_t x_remote = mapa_shared(stage0 + kOffX, peer);
     const uint32_t e_remote = mapa_shared(stage0 + kOffE, peer);
-    uint32_t xbar_remote[kXBufs], xfree_remote[kXBufs];
+    uint32_t xbar_remote[kXSets], xfree_remote[kXSets];
 #pragma unroll
-    for (int i = 0; i < kXBufs; ++i) {
+    for (int i = 0; i < kXSets; ++i) {
       xbar_remote[i] = mapa_shared(smem_u32(&sh.x_full[i]), peer);
       xfree_remote[i] = mapa_shared(smem_u32(&sh.x_free[i]), peer);
     }
@@ -411,7 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     // Step t uses exchange buffer t % 2 (this set's) in both CTAs.
     for (int j = set; ok && j < ntiles; j += 2) {
       const int sb = j % 2;
-      const int xb_i = j % kXBufs;
+      const int xb_i = j % kXSets;                      // this set's exchange barriers
       const int kbase = kbegin + j * kNk;
       const int cur0 = sl0, cur1 = sl1;
       if (j + 2 < ntiles) {
@@ -422,10 +440,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.s_full[sb], (j / 2) & 1, abort))) { ok = false; break; }
       tc_fence_after();
       float x[64];
-      tmem_ld32(tmem + lane_off + kColS, *reinterpret_cast<float(*)[32]>(&x[0]));
-      tmem_ld32(tmem + lane_off + kColS + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+      tmem_ld32(tmem + lane_off + kColS + sb * kNk, *reinterpret_cast<float(*)[32]>(&x[0]));
+      tmem_ld32(tmem + lane_off + kColS + sb * kNk + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
       tc_fence_before();
-      mbar_arrive(&sh.s_free[sb]);  // the S buffer may take the next step's scores
+      mbar_arrive(&sh.s_free[sb]);  // S buffer sb may take the scores of step j+2
       // encode own partial (block floating point) and send it; the own partial stays unrounded
       float am[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains: a 64-long max chain is latency-bound
 #pragma unroll
@@ -435,14 +453,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       const int e = block_exponent(amax * sl2);
       const float enc = sl2 * pow2i(14 - e);
       const uint64_t enc2 = f32x2(enc, enc), magic2 = f32x2(kMagic, kMagic);
-      // the peer must have read step j-2 out of the buffer before it is overwritten
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_free[xb_i], ((j - 2) / 2) & 1, abort, true))) {
+      // the peer must have read step j-1 (the other set's) out of the buffer before it is overwritten
+      if (j >= 1 && !__all_sync(0xffffffffu,
+                                mbar_wait_abortable(&sh.x_free[xb_i ^ 1], ((j - 1) / 2) & 1, abort, true))) {
         ok = false;
         break;
       }
       {
         // chunk-major buffer [8 chunks][128 rows][16 B]: a warp's store of one chunk is 512 contiguous bytes
-        const uint32_t xr = x_remote + xb_i * kXBytes + r * 16, br = xbar_remote[xb_i];
+        const uint32_t xr = x_remote + r * 16, br = xbar_remote[xb_i];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t w[4];
@@ -455,22 +474,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
           }
           st_async_v4(xr + c * (kTileRows * 16), make_uint4(w[0], w[1], w[2], w[3]), br);
         }
-        st_async_b32(e_remote + xb_i * kEBytes + r * 4, static_cast<uint32_t>(e), br);
+        st_async_b32(e_remote + r * 4, static_cast<uint32_t>(e), br);
       }
       // key mask of this step (past the split end or a slot outside the pool)
       const uint32_t masked0 = __ballot_sync(
           0xffffffffu, kbase + lane >= kend || cur0 < 0 || static_cast<int64_t>(cur0) >= p.pool_slots);
       const uint32_t masked1 = __ballot_sync(
           0xffffffffu, kbase + lane + 32 >= kend || cur1 < 0 || static_cast<int64_t>(cur1) >= p.pool_slots);
-      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_full[xb_i], (j / kXBufs) & 1, abort, true))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_full[xb_i], (j / kXSets) & 1, abort, true))) {
         ok = false;
         break;
       }
       // s = own * scale_log2 + peer (log2 units)
       float mx = -CUDART_INF_F;
       {
-        const uint8_t* xbp = smem + kOffX + xb_i * kXBytes + r * 16;
-        const int pe = *reinterpret_cast<const int*>(smem + kOffE + xb_i * kEBytes + r * 4);
+        const uint8_t* xbp = smem + kOffX + r * 16;
+        const int pe = *reinterpret_cast<const int*>(smem + kOffE + r * 4);
         const float pdec = pow2i(pe - 14), pm = -kMagic * pdec;
         const uint64_t pdec2 = f32x2(pdec, pdec), pm2 = f32x2(pm, pm), sl22 = f32x2(sl2, sl2);
 #pragma unroll
@@ -549,16 +568,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       f32x2_split(sq[0], s0, s1);
       f32x2_split(sq[1], s2, s3);
       l += (s0 + s1) + (s2 + s3);
-      // P buffer sb was last read by P.V of step j-2
-      if (j >= 2) {
+      // the P buffer was last read by P.V of step j-1
+      if (j >= 1) {
         if (!__all_sync(0xffffffffu,
-                        mbar_wait_abortable(&sh.k_empty[(j - 2) % kStages], ((j - 2) / kStages) & 1, abort))) {
+                        mbar_wait_abortable(&sh.k_empty[(j - 1) % kStages], ((j - 1) / kStages) & 1, abort))) {
           ok = false;
           break;
         }
         tc_fence_after();
       }
-      tmem_st32(tmem + lane_off + kColP + sb * (kNk / 2), pk);
+      tmem_st32(tmem + lane_off + kColP, pk);
       tc_fence_before();
       mbar_arrive(&sh.p_ready[sb]);
       // P.V(j), issued by the set's first thread once every row of P(j) is in
@@ -573,7 +592,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         if (pv_ok) {
           tc_fence_after();
           const uint64_t dv = desc_advance(d_v, (j % kStages) * kStageBytes);
-          const uint32_t pb = tmem + kColP + sb * (kNk / 2);
+          const uint32_t pb = tmem + kColP;
 #pragma unroll
           for (int ks = 0; ks < kNk / 16; ++ks)
             mma_ts(tmem + kColO, pb + ks * 8, desc_advance(dv, ks * 16 * 128), kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
