@@ -20,10 +20,11 @@
 // O_r += P . V_r for its own 256 v dims.  Every gathered row is read once per
 // pair and no MMA work is duplicated.
 //
-// Each softmax set owns one exchange buffer in each CTA (step t uses buffer
-// t % 2); before writing step t the sender waits until the receiver has read
-// step t-2 from it (a barrier in the sender that the receiver's warps arrive on
-// remotely).
+// Each CTA has one exchange buffer; step t is signalled on barrier pair t % 2
+// (one per softmax set).  Before writing step t the sender waits until the
+// receiver has read step t-1 out of it (a barrier in the sender that the
+// receiver's warps arrive on remotely).  A step is read out well before the
+// other set's next step is ready to send, so one buffer costs no waiting.
 //
 // Partial-score exchange format: per row and 64-key step, block floating point
 // -- one power-of-two exponent e with every |x| < 2^e and 64 int16 mantissas
@@ -40,14 +41,16 @@
 // the split merge, off by the same rounding).
 //
 // Per CTA (384 threads):
-//   warp 0      TMEM allocation; lane 0 issues the score MMAs S(t) once the
-//               stage is loaded and S(t-1) has been read out of the S buffer.
-//               A tcgen05.mma costs about 45 issue cycles whatever its shape,
-//               so each MMA is at least M=128 x N=64 (scores) or N=256 (P.V);
-//               the pipe takes the next MMA only about as fast as it runs one,
-//               so P.V is issued by the softmax set that wrote its P.
+//   warp 0      TMEM allocation; lane 0 issues the score MMAs S(t) into S
+//               buffer t % 2 once the stage is loaded and S(t-2) has been read
+//               out of that buffer, so the next scores are queued while the
+//               softmax reads the last ones.  A tcgen05.mma costs about 45
+//               issue cycles whatever its shape, so each MMA is at least
+//               M=128 x N=64 (scores) or N=256 (P.V); the pipe takes the next
+//               MMA only about as fast as it runs one, so P.V is issued by the
+//               softmax set that wrote its P.
 //   warps 1-3   producers: load the CTA's dims of 64 slot rows per step into a
-//               5-stage ring, the step's slot indices fetched one step ahead.
+//               5-stage ring, the step's slot indices fetched four steps ahead.
 //               A step whose 64 slots are consecutive (a compacted pool) is 5
 //               tiled TMA boxes of 64 rows.  A scattered step uses TMA
 //               tile::gather4 for latent blocks 0-2 (16 lanes of each producer
@@ -64,11 +67,12 @@
 //               running max of every row (step t waits for step t-1's); each
 //               set keeps its own row sums against the max it last used and
 //               the two are combined at the end.  O is rescaled in TMEM only
-//               when the running max grows by more than 8 (lazily).  A set
-//               frees the S buffer as soon as it has loaded S into registers
-//               and writes P (bf16) into P buffer t % 2, read from TMEM by P.V.
-// TMEM columns: O_r [0,256), S [256,320), P buffers 2 x 32 at [320,384),
-// Q_r latent [384,512).
+//               when the running max grows by more than 8 (lazily).  Set s
+//               reads S buffer s, frees it as soon as S is in registers, and
+//               writes P (bf16) into the one P buffer once P.V(t-1) is done.
+// TMEM columns: O_r [0,256), S buffers 2 x 64 at [256,384), P [384,416),
+// Q_r latent dims 0..191 [416,512); dims 192..255 of Q_r are read from shared
+// memory (16 KB, 128-byte swizzle), as are its rope dims.
 // Shared memory per stage: 4 latent blocks [64 keys][64 dims] (128-byte
 // swizzle, 8 KB each) + the CTA's rope block [64 keys][32 dims] (64-byte
 // swizzle, 4 KB).  The stage's lifetime runs from its load through S, the
@@ -232,9 +236,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
   if (warp == 0) {
     // ------------------------------------------------------------------ S issuer
     // The tensor pipe takes the next MMA only about as fast as it runs one, so a
-    // thread that also issued P.V could not react to the read-out of S while
-    // inside a P.V group: this thread issues only S, sleeping on the barrier it
-    // needs; each softmax set issues the P.V of its own steps.
+    // thread that also issued P.V could not react to a ready stage while inside
+    // a P.V group: this thread issues only S, sleeping on the barrier it needs;
+    // each softmax set issues the P.V of its own steps.
     if (lane == 0) {
       if (!mbar_wait_abortable(&sh.q_ready, 0, abort)) ok = false;
       fence_proxy_async_smem();  // Q rope dims were stored to shared memory by the softmax threads
