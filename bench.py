@@ -83,10 +83,14 @@ def job_throughput_gbs(kv_bytes_per_step, steps, world, max_ms):
     return kv_bytes_per_step * steps * world / (max_ms * 1e-3) / 1e9
 
 
-def workload_config(w, name, layout):
-    return {"workload": f"{name}: {wl.DESCRIPTIONS[name]}", "batch": w.batch, "prefix_len_total": int(w.prefix_len.sum()),
+def workload_config(w, name, layout, ragged=0):
+    desc = f"{name}: {wl.DESCRIPTIONS[name]}"
+    if ragged:
+        desc += f"; ragged trees, tree_len per request seeded U[{min(ragged, w.nodes)}, {w.nodes}]"
+    return {"workload": desc, "batch": w.batch, "prefix_len_total": int(w.prefix_len.sum()),
             "tree_nodes": w.nodes, "heads": w.heads, "d_qk": wl.D_QK, "d_v": wl.D_V, "pool_slots": w.pool_slots,
-            "slots": layout, "l2": "flushed before every step (256 MiB write)", "parallelism": "replicas"}
+            "slots": layout, "l2": "flushed before every step (256 MiB write)", "parallelism": "replicas",
+            **({"tree_len": [int(x) for x in w.tree_len]} if ragged else {})}
 
 
 class ClockSampler:
@@ -197,6 +201,12 @@ def run_ours(args, rank, world, local_rank):
     name = args.config
     layout = args.slots or wl.CONFIGS[name].slots
     w = wl.make_workload(name, slots=layout)
+    tl_dev = None
+    if args.ragged:
+        # ragged trees: request b keeps its first tree_len[b] nodes, tree_len seeded uniform in [MIN, T]
+        rng = np.random.default_rng(0xDD7EE0F0 + w.batch)
+        w.tree_len = rng.integers(min(args.ragged, w.nodes), w.nodes + 1, size=w.batch).astype(np.int32)
+        tl_dev = torch.from_numpy(w.tree_len).to(dev)
     d = wl.to_device(w, dev, poison=False)
     v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len, device=dev)
     out = torch.empty((w.batch, w.nodes, w.heads, wl.D_V), dtype=torch.float32, device=dev)
@@ -210,7 +220,7 @@ def run_ours(args, rank, world, local_rank):
     def step(ev, phase="all"):
         flush.fill_(1)                       # outside the step's events
         ev[0].record(stream)
-        v(*args_v, out=out, lse=lse, phase=phase)
+        v(*args_v, out=out, lse=lse, phase=phase, tree_len=tl_dev)
         ev[1].record(stream)
 
     for _ in range(args.warmup):
@@ -235,9 +245,10 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[1]) for e in events]
     # the dominant kernel alone, for its roofline: the prefix pass timed by its own events
+    # (ragged trees run as one call: there the "kernel" is the whole verify step)
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(min(args.steps, 50))]
     for ev in kev:
-        step(ev, phase="prefix")
+        step(ev, phase="all" if args.ragged else "prefix")
     torch.cuda.synchronize(dev)
     prefix_ms = [e[0].elapsed_time(e[1]) for e in kev]
     tot_ms = max_over_ranks(sum(step_ms), dev)
@@ -257,13 +268,15 @@ def run_ours(args, rank, world, local_rank):
         achieved, peak, unit = flops / prefix_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     else:
         achieved, peak, unit = w.algorithmic_bytes() / prefix_s / 1e9, peaks["hbm_gbs"], "GB/s"
-    traffic = recorded_traffic(name)
+    traffic = None if args.ragged else recorded_traffic(name)
 
     # end to end through the public API with host buffers
     e2e = None
     if rank >= 0:
         host = {k: d[k].cpu().pin_memory() for k in ("q", "slot_idx", "prefix_len", "tree_parent", "tree_slot_idx")}
-        dbuf = {k: torch.empty_like(d[k]) for k in host}
+        if tl_dev is not None:
+            host["tree_len"] = tl_dev.cpu().pin_memory()
+        dbuf = {k: torch.empty_like(host[k], device=dev) for k in host}
         h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
         h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -276,7 +289,7 @@ def run_ours(args, rank, world, local_rank):
             for k in host:
                 dbuf[k].copy_(host[k], non_blocking=True)
             v(dbuf["q"], d["kv_pool"], dbuf["slot_idx"], dbuf["prefix_len"], dbuf["tree_parent"],
-              dbuf["tree_slot_idx"], w.sm_scale, out=out, lse=lse)
+              dbuf["tree_slot_idx"], w.sm_scale, out=out, lse=lse, tree_len=dbuf.get("tree_len"))
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
             e1.record(stream)
@@ -290,9 +303,10 @@ def run_ours(args, rank, world, local_rank):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         s_per_row, rows_timed, threads = oracle_sample_rate(w, budget_s=args.cpu_budget)
-        step_s = s_per_row * w.batch * w.rows_per_request
+        active_rows = int(w.active_nodes().sum()) * w.heads
+        step_s = s_per_row * active_rows
         cpu = {"value": kv_bytes / step_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{rows_timed} of {w.batch * w.rows_per_request} rows of one step, "
+               "sample": f"{rows_timed} of {active_rows} rows of one step, "
                          f"time scaled by rows to a full step ({step_s:.1f} s)"}
 
     if rank == 0:
@@ -301,11 +315,12 @@ def run_ours(args, rank, world, local_rank):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w, name, layout),
+            "config": workload_config(w, name, layout, args.ragged),
             "us_per_step": {"mean": ms_per_step * 1e3, "median": statistics.median(us), "min": us[0]},
             "roofline_step": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (ms_per_step * 1e-3),
                               "bound": bound, "peaks": peak_kind},
-            "roofline": {"kernel": "prefix_pair_kernel", "bound": bound, "achieved": achieved, "peak": peak,
+            "roofline": {"kernel": "verify step (prefix + merge)" if args.ragged else "prefix_pair_kernel",
+                         "bound": bound, "achieved": achieved, "peak": peak,
                          "unit": unit, "frac": achieved / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} (burst)"},
             "gpu_launches": 2 * args.steps,
@@ -326,9 +341,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--ragged", type=int, default=0, metavar="MIN",
+                    help="ragged trees: request b keeps tree_len[b] ~ U[MIN, T] nodes (ddtree_verify_attn_ragged)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.ragged and args.impl == "reference":
+        ap.error("--ragged applies to --impl ours")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

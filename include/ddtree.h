@@ -62,6 +62,7 @@ typedef struct CUstream_st* ddt_stream_t;
 #define DDT_STATUS_BAD_PARENT 2    /* tree_parent[b][0] != -1 or tree_parent[b][i] not in [0, i): link ignored */
 #define DDT_STATUS_BAD_PREFIX 4    /* prefix_len[b] outside [0, max_prefix_len]: clamped */
 #define DDT_STATUS_TIMEOUT 8       /* a bounded on-chip wait gave up; outputs are not valid */
+#define DDT_STATUS_BAD_TREE_LEN 16 /* tree_len[b] outside [0, num_nodes]: clamped */
 
 /*
  * Sizes of one call.  Fixed by the library: D_qk = 576, D_v = 512.
@@ -118,6 +119,27 @@ DDT_API int ddtree_verify_attn(const void* q, const void* kv_pool, const int32_t
                        const int32_t* tree_slot_idx, float sm_scale, float* out, float* lse,
                        const ddt_dims* dims, void* workspace, size_t workspace_bytes,
                        ddt_stream_t stream);
+
+/*
+ * Ragged trees: the same call for a batch whose requests have different node
+ * counts (the pages' trees range from 9 to 65 nodes per request; "The Art of
+ * Systematic Investigation", section "Input Knowledge Required to Understand
+ * This Message", item 1).  Request b has tree_len[b] active nodes, 0..T-1 of
+ * its [T]-strided arrays; T = dims->num_nodes is the largest count and keeps
+ * every array's shape and stride.
+ *   tree_len   int32 [B] device, each in [0, T] (values outside are clamped and
+ *              set DDT_STATUS_BAD_TREE_LEN)
+ * Rows of active nodes get exactly what ddtree_verify_attn would give that
+ * request alone with T = tree_len[b]; rows of inactive nodes (t >= tree_len[b])
+ * get out = 0 and lse = -inf, and their parent, slot and q entries are never
+ * read.  Tiles of inactive rows skip the prefix pass.  tree_len must not be
+ * NULL when B > 0 (DDT_ERR_NULL).
+ */
+DDT_API int ddtree_verify_attn_ragged(const void* q, const void* kv_pool, const int32_t* slot_idx,
+                                      const int32_t* prefix_len, const int32_t* tree_parent,
+                                      const int32_t* tree_slot_idx, const int32_t* tree_len, float sm_scale,
+                                      float* out, float* lse, const ddt_dims* dims, void* workspace,
+                                      size_t workspace_bytes, ddt_stream_t stream);
 
 /*
  * The two phases of ddtree_verify_attn, for callers that schedule them

@@ -8,6 +8,7 @@ brute force below is an independent second reading of the same definition.
 Contents
   build()                 compile ddtree_oracle.c -> _build/libddtree_oracle.so (gcc, OpenMP)
   verify_attn(...)        fp64 verify attention via the C oracle (all rows or a row subset)
+  verify_attn_ragged(...) the same for requests with tree_len[b] <= T active nodes each
   tree_visibility(parent) the tree part of the visibility mask, via the C oracle
   kv_compact(...)         row-copy compaction via the C oracle
   brute_force(...)        NumPy fp64 re-derivation for tiny inputs (independent code path)
@@ -36,6 +37,7 @@ LIB = os.path.join(HERE, "_build", "libddtree_oracle.so")
 BAD_SLOT = 1
 BAD_PARENT = 2
 BAD_ARGS = 4
+BAD_TREE_LEN = 16
 
 _lib = None
 
@@ -107,6 +109,39 @@ def verify_attn(q_bits, pool_bits, slot_idx, prefix_len, tree_parent, tree_slot_
     if rows is None:
         out = out.reshape(B, T, H, dv)
         lse = lse.reshape(B, T, H)
+    return out, lse, st
+
+
+def verify_attn_ragged(q_bits, pool_bits, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, tree_len,
+                       lib=None):
+    """fp64 verify attention for a batch whose request b has tree_len[b] active nodes.
+
+    Request b is the request alone with T = tree_len[b] (its first tree_len[b]
+    nodes; nodes are in topological order, so every ancestor of an active node
+    is active); rows of nodes t >= tree_len[b] get out = 0, lse = -inf.  Values
+    of tree_len outside [0, T] are clamped and set BAD_TREE_LEN.  Arrays keep
+    their [B, T] shapes.
+    """
+    q = np.asarray(q_bits)
+    B, T, H, dqk = q.shape
+    dv = dqk - 64
+    out = np.zeros((B, T, H, dv), dtype=np.float64)
+    lse = np.full((B, T, H), -np.inf, dtype=np.float64)
+    st = 0
+    si = np.asarray(slot_idx).reshape(B, -1)
+    for b in range(B):
+        tl = int(tree_len[b])
+        if tl < 0 or tl > T:
+            st |= BAD_TREE_LEN
+            tl = min(max(tl, 0), T)
+        if tl == 0:
+            continue
+        o, l, s_b = verify_attn(q[b:b + 1, :tl], pool_bits, si[b:b + 1], np.asarray(prefix_len)[b:b + 1],
+                                np.asarray(tree_parent)[b:b + 1, :tl], np.asarray(tree_slot_idx)[b:b + 1, :tl],
+                                sm_scale, lib=lib)
+        out[b, :tl] = o[0]
+        lse[b, :tl] = l[0]
+        st |= s_b
     return out, lse, st
 
 

@@ -153,8 +153,8 @@ enum Phase : int { kPhasePrefix = 1, kPhaseMerge = 2 };
 
 int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t* slot_idx,
                   const int32_t* prefix_len, const int32_t* tree_parent, const int32_t* tree_slot_idx,
-                  float sm_scale, float* out, float* lse, const ddt_dims* dims, void* workspace,
-                  size_t workspace_bytes, ddt_stream_t stream) {
+                  const int32_t* tree_len, float sm_scale, float* out, float* lse, const ddt_dims* dims,
+                  void* workspace, size_t workspace_bytes, ddt_stream_t stream) {
   int rc = check_dims(dims);
   if (rc != DDT_OK) return rc;
   if (dims->batch == 0) return DDT_OK;
@@ -163,7 +163,7 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
     return DDT_ERR_NULL;
   if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(workspace, 256) || !aligned(slot_idx, 4) || !aligned(prefix_len, 4) ||
-      !aligned(tree_parent, 4) || !aligned(tree_slot_idx, 4))
+      !aligned(tree_parent, 4) || !aligned(tree_slot_idx, 4) || !aligned(tree_len, 4))
     return DDT_ERR_ALIGN;
   DeviceInfo dev;
   if ((rc = device_info(&dev)) != DDT_OK) return rc;
@@ -195,6 +195,9 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
       pp.pool_slots = dims->pool_slots;
       pp.slot_stride = dims->slot_stride;
       pp.rows = plan.rows;
+      pp.heads = dims->num_heads;
+      pp.nodes = dims->num_nodes;
+      pp.tree_len = tree_len;
       pp.row_tiles = plan.row_tiles;
       pp.chunk = plan.chunk;
       pp.max_splits = plan.splits;
@@ -216,6 +219,7 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
     tp.pool_slots = dims->pool_slots;
     tp.nodes = dims->num_nodes;
     tp.heads = dims->num_heads;
+    tp.tree_len = tree_len;
     tp.heads_per_cta = dims->num_heads < 8 ? dims->num_heads : 8;
     tp.row_tiles = plan.row_tiles;
     tp.chunk = plan.chunk;
@@ -239,11 +243,21 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
   const void *q, const void *kv_pool, const int32_t *slot_idx, const int32_t *prefix_len,                  \
       const int32_t *tree_parent, const int32_t *tree_slot_idx, float sm_scale, float *out, float *lse,      \
       const ddt_dims *dims, void *workspace, size_t workspace_bytes, ddt_stream_t stream
-#define DDT_VERIFY_PASS \
-  q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out, lse, dims, workspace, workspace_bytes, stream
+#define DDT_VERIFY_PASS                                                                                    \
+  q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, nullptr, sm_scale, out, lse, dims, workspace, \
+      workspace_bytes, stream
 
 extern "C" int ddtree_verify_attn(DDT_VERIFY_ARGS) {
   return verify_phases(kPhasePrefix | kPhaseMerge, DDT_VERIFY_PASS);
+}
+extern "C" int ddtree_verify_attn_ragged(const void* q, const void* kv_pool, const int32_t* slot_idx,
+                                         const int32_t* prefix_len, const int32_t* tree_parent,
+                                         const int32_t* tree_slot_idx, const int32_t* tree_len, float sm_scale,
+                                         float* out, float* lse, const ddt_dims* dims, void* workspace,
+                                         size_t workspace_bytes, ddt_stream_t stream) {
+  if (!tree_len && dims && dims->batch > 0) return DDT_ERR_NULL;
+  return verify_phases(kPhasePrefix | kPhaseMerge, q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx,
+                       tree_len, sm_scale, out, lse, dims, workspace, workspace_bytes, stream);
 }
 extern "C" int ddtree_verify_prefix_phase(DDT_VERIFY_ARGS) { return verify_phases(kPhasePrefix, DDT_VERIFY_PASS); }
 extern "C" int ddtree_verify_merge_phase(DDT_VERIFY_ARGS) { return verify_phases(kPhaseMerge, DDT_VERIFY_PASS); }

@@ -16,6 +16,7 @@ constexpr int32_t kStatusBadSlot = 1;
 constexpr int32_t kStatusBadParent = 2;
 constexpr int32_t kStatusBadPrefix = 4;
 constexpr int32_t kStatusTimeout = 8;
+constexpr int32_t kStatusBadTreeLen = 16;
 
 // Split-KV prefix pass: one CTA pair per (request, 128-row tile, key split).
 struct PrefixParams {
@@ -28,7 +29,10 @@ struct PrefixParams {
   const int32_t* prefix_len; // [B]
   int64_t pool_slots;
   int32_t slot_stride;
-  int32_t rows;              // T * H rows per request
+  int32_t rows;              // T * H rows per request (the row stride of q)
+  int32_t heads;             // H
+  int32_t nodes;             // T
+  const int32_t* tree_len;   // [B] active nodes per request, or null: all T active
   int32_t row_tiles;         // ceil(rows / 128)
   int32_t chunk;             // keys per split
   int32_t max_splits;        // split slots per request in the workspace
@@ -50,6 +54,7 @@ struct TailParams {
   int64_t pool_slots;
   int32_t nodes;                // T
   int32_t heads;                // H
+  const int32_t* tree_len;      // [B] active nodes per request, or null: all T active
   int32_t heads_per_cta;
   int32_t row_tiles;
   int32_t chunk;

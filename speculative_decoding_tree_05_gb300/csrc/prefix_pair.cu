@@ -167,6 +167,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
   }
   const int kbegin = split * p.chunk;
   if (kbegin >= L) return;  // both CTAs of the pair leave together
+  // ragged trees: only the rows of the request's first tree_len[b] nodes are computed
+  int rows_b = p.rows;
+  if (p.tree_len != nullptr) {
+    const int tl = __ldg(p.tree_len + b);
+    rows_b = (tl < 0 ? 0 : (tl > p.nodes ? p.nodes : tl)) * p.heads;  // out-of-range values: the merge reports them
+  }
+  if (row_tile * kTileRows >= rows_b) return;  // a tile of inactive rows: both CTAs leave together
   const int kend = min(L, kbegin + p.chunk);
   const int ntiles = (kend - kbegin + kNk - 1) / kNk;
 
@@ -214,7 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 #pragma unroll
   for (int i = 0; i < 2 * kSlotLookahead; ++i) pf[i] = producer ? fetch(i >> 1, i & 1) : -1;
   const int qrow = (warp & 3) * 32 + lane;
-  const bool q_valid = warp >= 4 && row_tile * kTileRows + qrow < p.rows;
+  const bool q_valid = warp >= 4 && row_tile * kTileRows + qrow < rows_b;
   const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(b) * p.rows + row_tile * kTileRows + qrow) * kDqk);
   uint4 qv[16 + 4];
 #pragma unroll
@@ -378,7 +385,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     const int r = (warp & 3) * 32 + lane;              // row of the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int grow = row_tile * kTileRows + r;
-    const bool row_valid = grow < p.rows;
+    const bool row_valid = grow < rows_b;
     float* hand = reinterpret_cast<float*>(smem + kOffHand);   // [2][128]
     float* fin = reinterpret_cast<float*>(smem + kOffFin);     // [2 sets][2][128]
 
@@ -644,7 +651,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         for (int it = 0; it < 8; ++it) {
           const int rr = 4 * it + (lane >> 3), u = lane & 7;  // row of the warp, 16-byte unit of the chunk
           const float4 v = *reinterpret_cast<const float4*>(stage_w + rr * 128 + ((u ^ (rr & 7)) << 4));
-          if (row0 + rr < p.rows)
+          if (row0 + rr < rows_b)
             *reinterpret_cast<float4*>(p.o_part + (prow0 + rr) * kDv + 256 * rank + 128 * set + c + 4 * u) = v;
         }
         __syncwarp();

@@ -48,6 +48,26 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
   const int T = p.nodes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+  // ragged trees: nodes t >= tree_len[b] are inactive (out = 0, lse = -inf);
+  // their parent and slot entries are never read
+  if (p.tree_len != nullptr) {
+    int tl = __ldg(p.tree_len + b);
+    if (tl < 0 || tl > T) {
+      if (t == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, kStatusBadTreeLen);
+      tl = tl < 0 ? 0 : T;
+    }
+    if (t >= tl) {
+      const int h = blockIdx.y * p.heads_per_cta + warp;
+      if (warp >= p.heads_per_cta || h >= p.heads) return;
+      const int64_t grow = (static_cast<int64_t>(b) * T + t) * p.heads + h;
+      float4* dst = reinterpret_cast<float4*>(p.out + grow * kDv);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dst[lane + 32 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane == 0) p.lse[grow] = -CUDART_INF_F;
+      return;
+    }
+  }
+
   // the request's parent and slot arrays, loaded in parallel, then one walk in smem
   for (int i = tid; i < T; i += kTailThreads) {
     par_sh[i] = __ldg(p.tree_parent + static_cast<int64_t>(b) * T + i);

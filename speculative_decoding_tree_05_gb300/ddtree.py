@@ -22,8 +22,10 @@ STATUS_BAD_SLOT = 1
 STATUS_BAD_PARENT = 2
 STATUS_BAD_PREFIX = 4
 STATUS_TIMEOUT = 8
+STATUS_BAD_TREE_LEN = 16
 
-EXPORTS = ("ddtree_verify_workspace_bytes", "ddtree_verify_attn", "ddtree_verify_prefix_phase",
+EXPORTS = ("ddtree_verify_workspace_bytes", "ddtree_verify_attn", "ddtree_verify_attn_ragged",
+           "ddtree_verify_prefix_phase",
            "ddtree_verify_merge_phase", "ddtree_verify_attn_static_scratch", "ddtree_kv_compact",
            "ddtree_read_device_status", "ddtree_status_string")
 
@@ -58,6 +60,9 @@ def lib():
             f.restype = ctypes.c_int
             f.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp, ctypes.POINTER(Dims), vp,
                           ctypes.c_size_t, vp]
+        L.ddtree_verify_attn_ragged.restype = ctypes.c_int
+        L.ddtree_verify_attn_ragged.argtypes = [vp, vp, i32p, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp,
+                                                ctypes.POINTER(Dims), vp, ctypes.c_size_t, vp]
         L.ddtree_verify_attn_static_scratch.restype = ctypes.c_int
         L.ddtree_verify_attn_static_scratch.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp,
                                                         ctypes.POINTER(Dims), vp]
@@ -117,14 +122,27 @@ class Verifier:
             self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device)
 
     def __call__(self, q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out=None,
-                 lse=None, stream=None, phase="all"):
-        """phase: "all" (ddtree_verify_attn), "prefix" or "merge" (the two halves of it)."""
+                 lse=None, stream=None, phase="all", tree_len=None):
+        """phase: "all" (ddtree_verify_attn), "prefix" or "merge" (the two halves of it).
+
+        tree_len: optional int32 [B] CUDA tensor of active nodes per request
+        (ddtree_verify_attn_ragged; phase must be "all").
+        """
         import torch
         B, T, H, D = q.shape
         if out is None:
             out = torch.empty((B, T, H, D_V), dtype=torch.float32, device=q.device)
         if lse is None:
             lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+        if tree_len is not None:
+            if phase != "all":
+                raise ValueError("ragged trees run as one call (phase='all')")
+            rc = lib().ddtree_verify_attn_ragged(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len),
+                                                 _ptr(tree_parent), _ptr(tree_slot_idx), _ptr(tree_len),
+                                                 float(sm_scale), _ptr(out), _ptr(lse), ctypes.byref(self.dims),
+                                                 _ptr(self.workspace), self.workspace.numel(), _stream(stream))
+            _check(rc, "ddtree_verify_attn_ragged")
+            return out, lse
         fn = {"all": "ddtree_verify_attn", "prefix": "ddtree_verify_prefix_phase",
               "merge": "ddtree_verify_merge_phase"}[phase]
         rc = getattr(lib(), fn)(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len), _ptr(tree_parent),

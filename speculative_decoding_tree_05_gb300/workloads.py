@@ -217,6 +217,13 @@ class Workload:
     q_bits: np.ndarray              # uint16 [B, T, H, 576] (bf16)
     kv_prefix_bits: list            # per request: uint16 [prefix_len[b], 576], logical order
     kv_tree_bits: np.ndarray        # uint16 [B, T, 576]: tree node rows
+    tree_len: np.ndarray | None = None  # int32 [B] active nodes per request (ragged trees), None: all T
+
+    def active_nodes(self) -> np.ndarray:
+        """Active tree nodes of each request (T everywhere unless the trees are ragged)."""
+        if self.tree_len is None:
+            return np.full(self.batch, self.nodes, dtype=np.int64)
+        return np.clip(np.asarray(self.tree_len, dtype=np.int64), 0, self.nodes)
 
     @property
     def rows_per_request(self) -> int:
@@ -227,17 +234,19 @@ class Workload:
         return int(self.prefix_len.max()) if self.batch else 0
 
     def kv_bytes(self) -> int:
-        """KV bytes one verify step must read: every prefix and tree row once."""
-        return int((int(self.prefix_len.sum()) + self.batch * self.nodes) * ROW_BYTES)
+        """KV bytes one verify step must read: every prefix and active tree row once."""
+        return int((int(self.prefix_len.sum()) + int(self.active_nodes().sum())) * ROW_BYTES)
 
     def flops(self) -> int:
         """Algorithmic FLOPs of the prefix contraction: 2*T*H*L*(576+512) per request."""
-        return int(2 * self.nodes * self.heads * int(self.prefix_len.sum()) * (D_QK + D_V))
+        t = self.active_nodes()
+        return int(2 * self.heads * int((t * self.prefix_len.astype(np.int64)).sum()) * (D_QK + D_V))
 
     def algorithmic_bytes(self) -> int:
-        """KV rows once + slot indices + q + out (fp32) + lse (fp32)."""
-        rows = self.batch * self.nodes * self.heads
-        return (self.kv_bytes() + int(self.prefix_len.sum()) * 4 + self.batch * self.nodes * 8
+        """KV rows once + slot indices + q + out (fp32) + lse (fp32), active rows only."""
+        nodes = int(self.active_nodes().sum())
+        rows = nodes * self.heads
+        return (self.kv_bytes() + int(self.prefix_len.sum()) * 4 + nodes * 8
                 + rows * ROW_BYTES + rows * D_V * 4 + rows * 4)
 
     def used_slots(self) -> np.ndarray:

@@ -343,3 +343,51 @@ def test_mutation_is_caught(name, tmp_path):
         except (AssertionError, ValueError, FloatingPointError):
             caught.append(pin.__name__)
     assert caught, f"mutation {name!r} passed every independent pin"
+
+
+# ----------------------------------------------------------------------------- ragged trees
+
+def test_ragged_rows_equal_the_full_tree_rows():
+    """Nodes are in topological order, so a node's ancestors precede it: cutting
+    a request's tree after tree_len nodes leaves every kept row unchanged (the
+    visibility rule of "The Art of Systematic Investigation", section "Input
+    Knowledge Required to Understand This Message", item 1), and the cut rows
+    are reported as out = 0, lse = -inf."""
+    c = case(41, T=7, H=2, L=(9, 0, 5))
+    lib = oracle.load()
+    out_u, lse_u, st_u = run(c, lib)
+    tree_len = np.asarray([7, 1, 4], np.int32)
+    out_r, lse_r, st_r = oracle.verify_attn_ragged(c["q_bits"], c["pool_bits"], c["slot_idx"], c["prefix_len"],
+                                                   c["tree_parent"], c["tree_slot_idx"], c["sm_scale"], tree_len,
+                                                   lib=lib)
+    assert st_u == 0 and st_r == 0
+    for b, tl in enumerate(tree_len):
+        np.testing.assert_allclose(out_r[b, :tl], out_u[b, :tl], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse_r[b, :tl], lse_u[b, :tl], rtol=0, atol=1e-13)
+        assert np.all(out_r[b, tl:] == 0.0) and np.all(np.isneginf(lse_r[b, tl:]))
+
+
+def test_ragged_matches_brute_force_on_the_cut_tree():
+    """The ragged result against the independent NumPy brute force run on each
+    request cut to its tree_len nodes."""
+    c = case(42, T=6, H=2, L=(5, 3))
+    tree_len = np.asarray([3, 6], np.int32)
+    out_r, lse_r, st = oracle.verify_attn_ragged(c["q_bits"], c["pool_bits"], c["slot_idx"], c["prefix_len"],
+                                                 c["tree_parent"], c["tree_slot_idx"], c["sm_scale"], tree_len)
+    assert st == 0
+    for b, tl in enumerate(tree_len):
+        ob, lb = oracle.brute_force(c["q_bits"][b:b + 1, :tl], c["pool_bits"], c["slot_idx"][b:b + 1],
+                                    c["prefix_len"][b:b + 1], c["tree_parent"][b:b + 1, :tl],
+                                    c["tree_slot_idx"][b:b + 1, :tl], c["sm_scale"])
+        np.testing.assert_allclose(out_r[b, :tl], ob[0], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse_r[b, :tl], lb[0], rtol=0, atol=1e-12)
+
+
+def test_ragged_tree_len_is_clamped_and_flagged():
+    c = case(43, T=4, H=1, L=(3, 2))
+    full = oracle.verify_attn_ragged(c["q_bits"], c["pool_bits"], c["slot_idx"], c["prefix_len"], c["tree_parent"],
+                                     c["tree_slot_idx"], c["sm_scale"], np.asarray([4, 0], np.int32))
+    bad = oracle.verify_attn_ragged(c["q_bits"], c["pool_bits"], c["slot_idx"], c["prefix_len"], c["tree_parent"],
+                                    c["tree_slot_idx"], c["sm_scale"], np.asarray([9, -2], np.int32))
+    assert full[2] == 0 and bad[2] == oracle.BAD_TREE_LEN
+    assert np.array_equal(full[0], bad[0]) and np.array_equal(full[1], bad[1])
