@@ -83,13 +83,14 @@ def job_throughput_gbs(kv_bytes_per_step, steps, world, max_ms):
     return kv_bytes_per_step * steps * world / (max_ms * 1e-3) / 1e9
 
 
-def workload_config(w, name, layout, ragged=0):
+def workload_config(w, name, layout, ragged=0, warm_l2=False):
     desc = f"{name}: {wl.DESCRIPTIONS[name]}"
     if ragged:
         desc += f"; ragged trees, tree_len per request seeded U[{min(ragged, w.nodes)}, {w.nodes}]"
     return {"workload": desc, "batch": w.batch, "prefix_len_total": int(w.prefix_len.sum()),
             "tree_nodes": w.nodes, "heads": w.heads, "d_qk": wl.D_QK, "d_v": wl.D_V, "pool_slots": w.pool_slots,
-            "slots": layout, "l2": "flushed before every step (256 MiB write)", "parallelism": "replicas",
+            "slots": layout, "parallelism": "replicas",
+            "l2": "warm: not flushed between steps" if warm_l2 else "flushed before every step (256 MiB write)",
             **({"tree_len": [int(x) for x in w.tree_len]} if ragged else {})}
 
 
@@ -218,7 +219,8 @@ def run_ours(args, rank, world, local_rank):
     # One step = one verify call (prefix pass + tail/merge, the latter a
     # programmatic dependent of the former, so no event may sit between them).
     def step(ev, phase="all"):
-        flush.fill_(1)                       # outside the step's events
+        if not args.warm_l2:
+            flush.fill_(1)                   # outside the step's events
         ev[0].record(stream)
         v(*args_v, out=out, lse=lse, phase=phase, tree_len=tl_dev)
         ev[1].record(stream)
@@ -283,7 +285,8 @@ def run_ours(args, rank, world, local_rank):
         d2h = h_out.numel() * 4 + h_lse.numel() * 4
         e2e_ms = []
         for i in range(args.warmup + max(10, args.steps // 10)):
-            flush.fill_(1)
+            if not args.warm_l2:
+                flush.fill_(1)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for k in host:
@@ -315,7 +318,7 @@ def run_ours(args, rank, world, local_rank):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w, name, layout, args.ragged),
+            "config": workload_config(w, name, layout, args.ragged, args.warm_l2),
             "us_per_step": {"mean": ms_per_step * 1e3, "median": statistics.median(us), "min": us[0]},
             "roofline_step": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (ms_per_step * 1e-3),
                               "bound": bound, "peaks": peak_kind},
@@ -341,6 +344,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--warm-l2", action="store_true",
+                    help="do not flush L2 between steps (a warm-L2 figure, labelled so in config.l2)")
     ap.add_argument("--ragged", type=int, default=0, metavar="MIN",
                     help="ragged trees: request b keeps tree_len[b] ~ U[MIN, T] nodes (ddtree_verify_attn_ragged)")
     args = ap.parse_args()
