@@ -77,3 +77,20 @@ def test_config_shapes_without_values():
     w = wl.make_workload("tiny")
     assert w.q_bits.shape == (1, 9, 16, 576) and w.prefix_len[0] == 256
     assert wl.tree_depths(w.tree_parent[0]).max() <= 4
+
+
+def test_work_formulas_count_active_rows_only():
+    """FLOPs 2*T*H*L*(576+512) and bytes per request; ragged trees count their active nodes."""
+    w = wl.make_workload("tiny", batch=3, prefix=("list", 100, 0, 37), nodes=5, heads=2, pool_slots=1 << 10)
+    L = w.prefix_len.astype(np.int64)
+    assert w.flops() == 2 * 5 * 2 * int(L.sum()) * 1088
+    assert w.kv_bytes() == (int(L.sum()) + 3 * 5) * 1152
+    rows = 3 * 5 * 2
+    assert w.algorithmic_bytes() == w.kv_bytes() + int(L.sum()) * 4 + 3 * 5 * 8 + rows * (1152 + 2048 + 4)
+    w.tree_len = np.asarray([5, 1, 7], np.int32)      # 7 is clamped to T = 5
+    t = np.asarray([5, 1, 5])
+    assert w.active_nodes().tolist() == t.tolist()
+    assert w.flops() == 2 * 2 * int((t * L).sum()) * 1088
+    assert w.kv_bytes() == (int(L.sum()) + int(t.sum())) * 1152
+    rows = int(t.sum()) * 2
+    assert w.algorithmic_bytes() == w.kv_bytes() + int(L.sum()) * 4 + int(t.sum()) * 8 + rows * (1152 + 2048 + 4)
