@@ -91,3 +91,16 @@ def test_read_status_null(lib):
 
 def test_workspace_bytes_bad_dims(lib):
     assert ddtree.workspace_bytes(dims(nodes=0)) == 0
+
+
+def test_ragged_host_checks(lib):
+    p = ctypes.c_void_p(0x10000)
+    d = dims(batch=2)
+
+    def ragged(tree_len, dd=d):
+        return lib.ddtree_verify_attn_ragged(p, p, p, p, p, p, tree_len, 0.1, p, p, ctypes.byref(dd), p, 1 << 30,
+                                             None)
+    assert ragged(None) == -1                       # tree_len is required when B > 0
+    assert ragged(ctypes.c_void_p(0x10002)) == -4   # misaligned int32 array
+    assert ragged(None, dims(batch=0)) == 0         # empty batch: nothing enqueued
+    assert ragged(p, dims(heads=0)) == -2
