@@ -209,7 +209,9 @@ def run_ours(args, rank, world, local_rank):
         w.tree_len = rng.integers(min(args.ragged, w.nodes), w.nodes + 1, size=w.batch).astype(np.int32)
         tl_dev = torch.from_numpy(w.tree_len).to(dev)
     d = wl.to_device(w, dev, poison=False)
-    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len, device=dev)
+    # the host knows the prefix lengths of its batch: the sum steers the key-split length
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len, device=dev,
+                        prefix_len_sum=int(w.prefix_len.sum()))
     out = torch.empty((w.batch, w.nodes, w.heads, wl.D_V), dtype=torch.float32, device=dev)
     lse = torch.empty((w.batch, w.nodes, w.heads), dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)

@@ -72,10 +72,19 @@ typedef struct CUstream_st* ddt_stream_t;
  *   pool_slots     N >= 1 rows in the KV pool
  *   slot_stride    row stride (in entries) of slot_idx, >= max_prefix_len
  *   max_prefix_len upper bound on every prefix_len[b]; it sizes the workspace
- *                  and the launch.  The key-range split of each request depends
- *                  only on this value, the device's SM count and prefix_len[b],
- *                  never on slot addresses, so results are bitwise reproducible
- *                  and identical for any slot layout of the same logical data.
+ *                  and the launch.
+ *   prefix_len_sum optional host-side hint: the sum of prefix_len over the
+ *                  batch, or 0 if unknown.  It only steers the choice of the
+ *                  key-split length (with 0 the planner assumes every request
+ *                  is max_prefix_len long, which over-counts the work units of
+ *                  a batch of mixed lengths and picks longer splits than
+ *                  needed); results are correct for any value.  The workspace
+ *                  size depends on it, so query ddtree_verify_workspace_bytes
+ *                  with the same dims that the calls use.
+ * The key-range split of each request depends only on these sizes, the
+ * device's SM count and prefix_len[b], never on slot addresses, so results are
+ * bitwise reproducible and identical for any slot layout of the same logical
+ * data.
  */
 typedef struct {
   int32_t batch;
@@ -84,7 +93,7 @@ typedef struct {
   int32_t slot_stride;
   int64_t pool_slots;
   int32_t max_prefix_len;
-  int32_t reserved;
+  int32_t prefix_len_sum;
 } ddt_dims;
 
 /* Bytes of workspace ddtree_verify_attn needs for these sizes on the current

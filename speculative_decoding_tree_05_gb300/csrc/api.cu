@@ -73,6 +73,10 @@ int make_plan(const ddt_dims* d, int sm_count, Plan* plan) {
     // fewest splits.  Splits are at least kMinChunk keys long.
     const int64_t pairs = sm_count >= 2 ? sm_count / 2 : 1;
     const int64_t per_split = int64_t(d->batch) * p.row_tiles;
+    // Units that hold keys: without a hint every request is taken to be L
+    // long; with the sum of the prefix lengths, a request has about
+    // sum/chunk splits in all plus half a split each for its partial last one.
+    const int64_t len_sum = d->prefix_len_sum > 0 ? std::min<int64_t>(d->prefix_len_sum, L * d->batch) : 0;
     const int64_t tiles = (L + kKeysPerTile - 1) / kKeysPerTile;
     const int64_t max_splits = std::max<int64_t>(1, std::min<int64_t>(64, (L + kMinChunk - 1) / kMinChunk));
     int64_t best = 1;
@@ -80,7 +84,12 @@ int make_plan(const ddt_dims* d, int sm_count, Plan* plan) {
     for (int64_t s = 1; s <= max_splits; ++s) {
       const int64_t steps = (tiles + s - 1) / s;            // per unit
       const int64_t splits = (tiles + steps - 1) / steps;   // splits that actually hold keys
-      const int64_t waves = (per_split * splits + pairs - 1) / pairs;
+      int64_t units = per_split * splits;
+      if (len_sum > 0) {
+        const int64_t chunk_keys = steps * kKeysPerTile;
+        units = std::min(units, p.row_tiles * ((len_sum + chunk_keys - 1) / chunk_keys + (d->batch + 1) / 2));
+      }
+      const int64_t waves = (units + pairs - 1) / pairs;
       const int64_t cost = waves * (steps + kUnitOverheadSteps);
       if (best_cost < 0 || cost < best_cost) {
         best_cost = cost;

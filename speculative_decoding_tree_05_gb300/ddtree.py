@@ -39,7 +39,7 @@ class DDTError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("num_nodes", ctypes.c_int32), ("num_heads", ctypes.c_int32),
                 ("slot_stride", ctypes.c_int32), ("pool_slots", ctypes.c_int64),
-                ("max_prefix_len", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("max_prefix_len", ctypes.c_int32), ("prefix_len_sum", ctypes.c_int32)]
 
 
 _lib = None
@@ -90,8 +90,10 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def make_dims(batch, nodes, heads, pool_slots, slot_stride, max_prefix_len) -> Dims:
-    return Dims(int(batch), int(nodes), int(heads), int(slot_stride), int(pool_slots), int(max_prefix_len), 0)
+def make_dims(batch, nodes, heads, pool_slots, slot_stride, max_prefix_len, prefix_len_sum=0) -> Dims:
+    """prefix_len_sum: optional host-side sum of the prefix lengths (0: unknown); it only steers the split."""
+    return Dims(int(batch), int(nodes), int(heads), int(slot_stride), int(pool_slots), int(max_prefix_len),
+                int(prefix_len_sum))
 
 
 def workspace_bytes(dims: Dims) -> int:
@@ -110,10 +112,11 @@ class Verifier:
     tree_parent [B,T] int32, tree_slot_idx [B,T] int32 -- all CUDA tensors.
     """
 
-    def __init__(self, batch, nodes, heads, pool_slots, slot_stride, max_prefix_len=None, device=None):
+    def __init__(self, batch, nodes, heads, pool_slots, slot_stride, max_prefix_len=None, device=None,
+                 prefix_len_sum=0):
         import torch
         self.dims = make_dims(batch, nodes, heads, pool_slots, slot_stride,
-                              slot_stride if max_prefix_len is None else max_prefix_len)
+                              slot_stride if max_prefix_len is None else max_prefix_len, prefix_len_sum)
         self.device = torch.device("cuda") if device is None else torch.device(device)
         with torch.cuda.device(self.device):
             n = workspace_bytes(self.dims)

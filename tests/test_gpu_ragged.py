@@ -109,3 +109,21 @@ def test_multi_request_128_heads_65_nodes_sampled():
     l = lse.reshape(-1)[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
     e_o, e_l = np.abs(o - ref_o), np.abs(l - ref_l)
     assert e_o.max() <= OUT_MAX and e_o.mean() <= OUT_MEAN and e_l.max() <= LSE_MAX, (e_o.max(), e_l.max())
+
+
+def test_prefix_len_sum_hint_changes_only_the_split():
+    """The host-side sum of the prefix lengths steers the split length of a batch
+    of mixed lengths; the result matches the oracle with and without it."""
+    w = wl.make_workload("tiny", batch=4, prefix=("list", 20000, 700, 6000, 150), nodes=9, heads=16,
+                         pool_slots=1 << 16, slots="churn")
+    d = wl.to_device(w, "cuda", poison=True)
+    pool, si, ts = w.compact_host_pool()
+    ref_o, ref_l, st = oracle.verify_attn(w.q_bits, pool, si, w.prefix_len, w.tree_parent, ts, w.sm_scale)
+    assert st == 0
+    for hint in (0, int(w.prefix_len.sum())):
+        v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len,
+                            prefix_len_sum=hint)
+        out, lse = v(*_args(d, w))
+        torch.cuda.synchronize()
+        assert v.status() == 0
+        _check_active(out, lse, ref_o, ref_l, [w.nodes] * w.batch)
