@@ -156,8 +156,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
   // it then occupies only SMs freed by finished CTAs and waits for this grid
   // to complete before it reads the partials
   grid_dep_launch();
-  const int split = blockIdx.x >> 1;
-  const int row_tile = blockIdx.y;
+  // x: the pair of a 128-row tile, y: the key split.  CTAs are dispatched in
+  // x-fastest order, so the pairs of one wave share one or two key ranges:
+  // their rows stay in L2 instead of every wave re-reading the whole prefix
+  // from HBM.
+  const int row_tile = blockIdx.x >> 1;
+  const int split = blockIdx.y;
   const int b = blockIdx.z;
 
   int L = __ldg(p.prefix_len + b);
@@ -691,7 +695,7 @@ cudaError_t configure_prefix() {
 }
 
 cudaError_t launch_prefix(const PrefixParams& p, int batch, int splits, cudaStream_t stream) {
-  dim3 grid(2 * splits, p.row_tiles, batch);
+  dim3 grid(2 * p.row_tiles, splits, batch);
   prefix_pair_kernel<<<grid, kThreads, kSmem, stream>>>(p);
   return cudaGetLastError();
 }
