@@ -10,8 +10,13 @@ divided by the device time of the steps).  Under torchrun each rank runs an
 independent replica of the workload (weak scaling; no collective exists on
 this path).
 
+The default workload is c5 (8 requests, ~540k prefix keys, 8M-slot pool), the
+largest configuration that fits one GPU; c2, c3 and c4 are timed in the same
+run with the same protocol and reported under "per_config".
+
 --impl reference times the fp64 CPU oracle (the only reference this project
-has) on the host cores, on a bounded sample of the same workload.
+has) on the host cores: whole verify steps of the same workload, as many as
+fit in a time cap.
 """
 from __future__ import annotations
 
@@ -162,30 +167,38 @@ def oracle_sample_rate(w, budget_s=8.0, min_rows=8):
 
 
 def run_reference(args, rank, world):
+    """The fp64 oracle on the host cores, whole verify steps of the same workload.
+
+    A whole step of the larger configurations takes seconds to tens of seconds
+    on the host, so the run is capped: one untimed warm-up step, then timed
+    steps until K are done or --ref-budget seconds of timed work have passed
+    (at least one).  The line reports the steps actually timed.
+    """
     if rank != 0:
         return
     name = args.config
     w = wl.make_workload(name)
-    total = w.batch * w.rows_per_request
     kv_bytes = w.kv_bytes()
     import oracle
     oracle.load()
-    rng = np.random.default_rng(77)
-    per_step_rows = max(1, min(total, args.ref_rows))
     times = []
-    for step in range(args.warmup + args.steps):
-        rows = np.sort(rng.choice(total, size=per_step_rows, replace=False))
+    warm = 1
+    for step in range(warm + args.steps):
         t0 = time.perf_counter()
-        oracle.verify_workload(w, rows=rows)
-        dt = (time.perf_counter() - t0) * total / per_step_rows   # scaled to the whole step
-        if step >= args.warmup:
+        oracle.verify_workload(w)
+        dt = time.perf_counter() - t0
+        if step >= warm:
             times.append(dt)
+            if sum(times) >= args.ref_budget:
+                break
     step_s = statistics.mean(times)
     value = kv_bytes / step_s / 1e9
     cores = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
-    sample = f"{per_step_rows} of {total} rows per step, time scaled by rows to a full step"
-    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+    sample = (f"whole verify steps ({w.batch * w.rows_per_request} rows); {len(times)} timed of {args.steps} "
+              f"requested after {warm} warm-up (capped at {args.ref_budget:.0f} s of timed work)")
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": len(times),
+            "warmup": warm, "requested": {"steps": args.steps, "warmup": args.warmup},
+            "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": workload_config(w, name, wl.CONFIGS[name].slots),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
@@ -193,20 +206,33 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local_rank):
+def roofline_of(w, kernel_s, peaks):
+    """Roofline of the dominant kernel from its algorithmic work and measured duration."""
+    hbm = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    flops = w.flops()
+    bound = "tensor" if flops / tc >= w.algorithmic_bytes() / hbm else "hbm"
+    if bound == "tensor":
+        return bound, flops / kernel_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    return bound, w.algorithmic_bytes() / kernel_s / 1e9, peaks["hbm_gbs"], "GB/s"
+
+
+def time_config(name, args, dev, world, layout=None, ragged=0, flush=None):
+    """Device time of verify steps on one configuration (inputs resident in HBM).
+
+    Returns a dict with the workload, its tensors and the measured times; the
+    caller decides what else to measure.
+    """
     import torch
     from speculative_decoding_tree_05_gb300 import ddtree
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    name = args.config
-    layout = args.slots or wl.CONFIGS[name].slots
+    layout = layout or wl.CONFIGS[name].slots
     w = wl.make_workload(name, slots=layout)
     tl_dev = None
-    if args.ragged:
+    if ragged:
         # ragged trees: request b keeps its first tree_len[b] nodes, tree_len seeded uniform in [MIN, T]
         rng = np.random.default_rng(0xDD7EE0F0 + w.batch)
-        w.tree_len = rng.integers(min(args.ragged, w.nodes), w.nodes + 1, size=w.batch).astype(np.int32)
+        w.tree_len = rng.integers(min(ragged, w.nodes), w.nodes + 1, size=w.batch).astype(np.int32)
         tl_dev = torch.from_numpy(w.tree_len).to(dev)
     d = wl.to_device(w, dev, poison=False)
     # the host knows the prefix lengths of its batch: the sum steers the key-split length
@@ -214,7 +240,6 @@ def run_ours(args, rank, world, local_rank):
                         prefix_len_sum=int(w.prefix_len.sum()))
     out = torch.empty((w.batch, w.nodes, w.heads, wl.D_V), dtype=torch.float32, device=dev)
     lse = torch.empty((w.batch, w.nodes, w.heads), dtype=torch.float32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     args_v = (d["q"], d["kv_pool"], d["slot_idx"], d["prefix_len"], d["tree_parent"], d["tree_slot_idx"], w.sm_scale)
 
@@ -231,8 +256,59 @@ def run_ours(args, rank, world, local_rank):
         step([torch.cuda.Event(enable_timing=True) for _ in range(2)])
     torch.cuda.synchronize(dev)
     assert v.status() == 0
+    return dict(w=w, d=d, v=v, out=out, lse=lse, stream=stream, step=step, tl_dev=tl_dev, layout=layout)
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+
+def timed_steps(cfg, n):
+    import torch
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for ev in events:
+        cfg["step"](ev)
+    return events
+
+
+def kernel_ms(cfg, n, ragged):
+    """The dominant kernel alone (the prefix pass, by its own events; ragged trees
+    run as one call, so there the whole verify step)."""
+    import torch
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for ev in kev:
+        cfg["step"](ev, phase="all" if ragged else "prefix")
+    torch.cuda.synchronize()
+    return [e[0].elapsed_time(e[1]) for e in kev]
+
+
+def summary_of(cfg, step_ms, prefix_ms, peaks, peak_kind, ragged=0):
+    w = cfg["w"]
+    hbm = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    ms = statistics.mean(step_ms)
+    us = sorted(x * 1e3 for x in step_ms)
+    t_roof = max(w.algorithmic_bytes() / hbm, w.flops() / tc)
+    bound, achieved, peak, unit = roofline_of(w, statistics.mean(prefix_ms) * 1e-3, peaks)
+    return {
+        "us_per_step": {"mean": ms * 1e3, "median": statistics.median(us), "min": us[0]},
+        "kv_gbs": w.kv_bytes() / (ms * 1e-3) / 1e9,
+        "roofline_step": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (ms * 1e-3), "bound": bound,
+                          "peaks": peak_kind},
+        "roofline": {"kernel": "verify step (prefix + merge)" if ragged else "prefix_pair_kernel",
+                     "bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "traffic": None if ragged else recorded_traffic(w.name),
+                     "peak_kind": f"{peak_kind} (burst)", "kernel_us": statistics.mean(prefix_ms) * 1e3},
+    }
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    name = args.config
+    peaks, peak_kind = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cfg = time_config(name, args, dev, world, layout=args.slots, ragged=args.ragged, flush=flush)
+    w, d, v, out, lse, stream = cfg["w"], cfg["d"], cfg["v"], cfg["out"], cfg["lse"], cfg["stream"]
+
     clocks = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
@@ -240,70 +316,63 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.3)   # let the sampler start before the timed region
     wall0 = time.perf_counter()
-    for ev in events:
-        step(ev)
+    events = timed_steps(cfg, args.steps)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[1]) for e in events]
-    # the dominant kernel alone, for its roofline: the prefix pass timed by its own events
-    # (ragged trees run as one call: there the "kernel" is the whole verify step)
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(min(args.steps, 50))]
-    for ev in kev:
-        step(ev, phase="all" if args.ragged else "prefix")
-    torch.cuda.synchronize(dev)
-    prefix_ms = [e[0].elapsed_time(e[1]) for e in kev]
+    prefix_ms = kernel_ms(cfg, min(args.steps, 50), args.ragged)
     tot_ms = max_over_ranks(sum(step_ms), dev)
     kv_bytes = w.kv_bytes()
     value = job_throughput_gbs(kv_bytes, args.steps, world, tot_ms)
     ms_per_step = tot_ms / args.steps
-
-    # roofline of the step and of the prefix kernel (dominant)
-    peaks, peak_kind = load_peaks()
-    hbm = peaks["hbm_gbs"] * 1e9
-    tc = peaks["bf16_tflops"] * 1e12
-    flops = w.flops()
-    t_roof = max(w.algorithmic_bytes() / hbm, flops / tc)
-    prefix_s = statistics.mean(prefix_ms) * 1e-3
-    bound = "tensor" if flops / tc >= w.algorithmic_bytes() / hbm else "hbm"
-    if bound == "tensor":
-        achieved, peak, unit = flops / prefix_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-    else:
-        achieved, peak, unit = w.algorithmic_bytes() / prefix_s / 1e9, peaks["hbm_gbs"], "GB/s"
-    traffic = None if args.ragged else recorded_traffic(name)
+    summ = summary_of(cfg, step_ms, prefix_ms, peaks, peak_kind, args.ragged)
 
     # end to end through the public API with host buffers
-    e2e = None
-    if rank >= 0:
-        host = {k: d[k].cpu().pin_memory() for k in ("q", "slot_idx", "prefix_len", "tree_parent", "tree_slot_idx")}
-        if tl_dev is not None:
-            host["tree_len"] = tl_dev.cpu().pin_memory()
-        dbuf = {k: torch.empty_like(host[k], device=dev) for k in host}
-        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = h_out.numel() * 4 + h_lse.numel() * 4
-        e2e_ms = []
-        for i in range(args.warmup + max(10, args.steps // 10)):
-            if not args.warm_l2:
-                flush.fill_(1)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for k in host:
-                dbuf[k].copy_(host[k], non_blocking=True)
-            v(dbuf["q"], d["kv_pool"], dbuf["slot_idx"], dbuf["prefix_len"], dbuf["tree_parent"],
-              dbuf["tree_slot_idx"], w.sm_scale, out=out, lse=lse, tree_len=dbuf.get("tree_len"))
-            h_out.copy_(out, non_blocking=True)
-            h_lse.copy_(lse, non_blocking=True)
-            e1.record(stream)
-            e1.synchronize()
-            if i >= args.warmup:
-                e2e_ms.append(e0.elapsed_time(e1))
-        e2e_s = statistics.mean(e2e_ms) * 1e-3
-        e2e = {"value": kv_bytes * world / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3}
+    host = {k: d[k].cpu().pin_memory() for k in ("q", "slot_idx", "prefix_len", "tree_parent", "tree_slot_idx")}
+    if cfg["tl_dev"] is not None:
+        host["tree_len"] = cfg["tl_dev"].cpu().pin_memory()
+    dbuf = {k: torch.empty_like(host[k], device=dev) for k in host}
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    e2e_ms = []
+    for i in range(args.warmup + max(10, args.steps // 10)):
+        if not args.warm_l2:
+            flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        v(dbuf["q"], d["kv_pool"], dbuf["slot_idx"], dbuf["prefix_len"], dbuf["tree_parent"],
+          dbuf["tree_slot_idx"], w.sm_scale, out=out, lse=lse, tree_len=dbuf.get("tree_len"))
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_s = statistics.mean(e2e_ms) * 1e-3
+    e2e = {"value": kv_bytes * world / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3}
+    del cfg, d, v, dbuf, host
+
+    # the other configurations, same protocol, reported under per_config
+    per_config = {}
+    extra = [c for c in (args.also.split(",") if args.also else []) if c and c != name]
+    for other in extra:
+        oc = time_config(other, args, dev, world, flush=flush)
+        oev = timed_steps(oc, args.steps)
+        torch.cuda.synchronize(dev)
+        oms = [e[0].elapsed_time(e[1]) for e in oev]
+        okm = kernel_ms(oc, min(args.steps, 50), 0)
+        per_config[other] = {"workload": f"{other}: {wl.DESCRIPTIONS[other]}",
+                             **summary_of(oc, oms, okm, peaks, peak_kind)}
+        del oc
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -315,22 +384,18 @@ def run_ours(args, rank, world, local_rank):
                          f"time scaled by rows to a full step ({step_s:.1f} s)"}
 
     if rank == 0:
-        us = sorted(x * 1e3 for x in step_ms)
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w, name, layout, args.ragged, args.warm_l2),
-            "us_per_step": {"mean": ms_per_step * 1e3, "median": statistics.median(us), "min": us[0]},
-            "roofline_step": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (ms_per_step * 1e-3),
-                              "bound": bound, "peaks": peak_kind},
-            "roofline": {"kernel": "verify step (prefix + merge)" if args.ragged else "prefix_pair_kernel",
-                         "bound": bound, "achieved": achieved, "peak": peak,
-                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
-                         "peak_kind": f"{peak_kind} (burst)"},
+            "config": workload_config(w, name, args.slots or wl.CONFIGS[name].slots, args.ragged, args.warm_l2),
+            "us_per_step": summ["us_per_step"],
+            "roofline_step": summ["roofline_step"],
+            "roofline": summ["roofline"],
             "gpu_launches": 2 * args.steps,
             "clocks": clk, "wall_s": wall,
             "e2e": e2e, "cpu_baseline": cpu,
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
 
@@ -341,11 +406,15 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=sorted(wl.CONFIGS), default="c2")
+    ap.add_argument("--config", choices=sorted(wl.CONFIGS), default="c5",
+                    help="the measured workload (default c5, the largest configuration that fits one GPU)")
+    ap.add_argument("--also", default="c2,c3,c4",
+                    help="comma-separated configurations also timed in the same run (per_config); '' for none")
     ap.add_argument("--slots", choices=["perm", "churn", "contiguous"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--ref-budget", type=float, default=90.0,
+                    help="--impl reference: seconds of timed oracle work after which no further step starts")
     ap.add_argument("--warm-l2", action="store_true",
                     help="do not flush L2 between steps (a warm-L2 figure, labelled so in config.l2)")
     ap.add_argument("--ragged", type=int, default=0, metavar="MIN",

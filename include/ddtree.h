@@ -56,6 +56,7 @@ typedef struct CUstream_st* ddt_stream_t;
 #define DDT_ERR_ALIGN (-4)     /* a device pointer is not 16-byte aligned */
 #define DDT_ERR_LAUNCH (-5)    /* a kernel launch or CUDA runtime call failed */
 #define DDT_ERR_DEVICE (-6)    /* the current device is not an sm_103 GPU */
+#define DDT_ERR_ALIAS (-7)     /* ddtree_kv_compact_check: destinations overlap or cover a live row */
 
 /* Device status bits (ddtree_read_device_status). */
 #define DDT_STATUS_BAD_SLOT 1      /* a slot index outside [0, pool_slots): key left out */
@@ -184,7 +185,8 @@ DDT_API int ddtree_verify_merge_phase(const void* q, const void* kv_pool, const 
  * for j < prefix_len[b].  Entries of slot_idx_out beyond prefix_len[b] are not
  * written.  kv_src and kv_dst both have dims->pool_slots rows and may be the
  * same pool only if no destination row [dst_start[b], dst_start[b]+prefix_len[b])
- * is a source row of any request (the caller's contract; not checked).
+ * is a source row of any request (the caller's contract; ddtree_kv_compact
+ * does not check it -- ddtree_kv_compact_check below does, on the host).
  *   dst_start   int64 [B] device
  *   workspace   >= 256 bytes, 256-byte aligned (status word; bad source or
  *               destination slots set DDT_STATUS_BAD_SLOT and skip the row)
@@ -192,6 +194,29 @@ DDT_API int ddtree_verify_merge_phase(const void* q, const void* kv_pool, const 
 DDT_API int ddtree_kv_compact(const void* kv_src, void* kv_dst, const int32_t* slot_idx,
                       const int32_t* prefix_len, const int64_t* dst_start, int32_t* slot_idx_out,
                       const ddt_dims* dims, void* workspace, ddt_stream_t stream);
+
+/*
+ * Debug validator of ddtree_kv_compact's aliasing contract, run on HOST copies
+ * of the tables before a compaction ("The Architecture Detective", section
+ * "Defragmentation: Separating Signal from Noise": compacting live KV in place
+ * is only safe if no copy overwrites a row that is still read).  Pure host code:
+ * it needs no GPU and enqueues nothing.
+ *   slot_idx       int32 [B, slot_stride] host, as passed to ddtree_kv_compact
+ *   prefix_len     int32 [B] host, each in [0, max_prefix_len] (else DDT_ERR_DIMS)
+ *   dst_start      int64 [B] host
+ *   tree_slot_idx  int32 [B, num_nodes] host, or NULL: the requests' tree rows,
+ *                  which an in-place compaction must not overwrite either
+ *   same_pool      nonzero when kv_dst is kv_src (in-place compaction)
+ *   bad_slot       optional out: the first offending slot, or -1
+ * Returns DDT_OK when every destination range [dst_start[b], +prefix_len[b])
+ * lies inside the pool and the ranges are pairwise disjoint, and, for
+ * same_pool, no destination row is a source slot of any request (a row that
+ * is already at its destination, slot_idx[b][j] == dst_start[b] + j, is
+ * allowed) or a tree slot; DDT_ERR_ALIAS otherwise.
+ */
+DDT_API int ddtree_kv_compact_check(const int32_t* slot_idx, const int32_t* prefix_len, const int64_t* dst_start,
+                                    const int32_t* tree_slot_idx, const ddt_dims* dims, int32_t same_pool,
+                                    int64_t* bad_slot);
 
 /*
  * Verify attention without any allocation, for callers that cannot allocate
@@ -204,8 +229,13 @@ DDT_API int ddtree_kv_compact(const void* kv_src, void* kv_dst, const int32_t* s
  * GPU that loads the library holds until the process exits.  Sizes whose
  * scratch (ddtree_verify_workspace_bytes) exceeds 32 MiB return
  * DDT_ERR_WORKSPACE before anything is enqueued.  The first call on each device
- * looks up the array's device address (once, with that device current); make
- * that first call before any stream capture.  Every call shares the one array:
+ * looks up the array's device address (once, with that device current).  That
+ * lookup can be the moment CUDA loads the library's device code onto the device
+ * and reserves the array (modules load lazily by default), so it may allocate:
+ * make the first call on each device at start-up, outside any allocator
+ * callback and before any stream capture; later calls allocate nothing.  Size,
+ * device and pointer checks return the same codes as ddtree_verify_attn.
+ * Every call shares the one array:
  * calls whose work overlaps on the GPU (on different streams, or from several
  * threads) race and must be serialised by the caller.  The device status word
  * of these calls is not readable by the caller.
@@ -216,7 +246,10 @@ DDT_API int ddtree_verify_attn_static_scratch(const void* q, const void* kv_pool
                                               float* lse, const ddt_dims* dims, ddt_stream_t stream);
 
 /* Waits for `stream`, then copies the status word of the last call that used
- * `workspace` to *host_status.  Returns DDT_OK or DDT_ERR_*. */
+ * `workspace` to *host_status.  Returns DDT_OK or DDT_ERR_*.  The kernels write
+ * the word asynchronously on the stream the verify call was enqueued on, so
+ * the read waits for that stream alone (not the whole device): work on other
+ * streams keeps running. */
 DDT_API int ddtree_read_device_status(const void* workspace, int32_t* host_status, ddt_stream_t stream);
 
 /* Static text for a DDT_ERR_* return code. */

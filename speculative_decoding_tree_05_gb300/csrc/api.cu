@@ -2,7 +2,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <algorithm>
+#include <cstdint>
 #include <mutex>
+#include <utility>
+#include <vector>
 #include "../../include/ddtree.h"
 #include "kernels.cuh"
 
@@ -147,6 +150,24 @@ bool encode_pool_map(CUtensorMap* m, const void* pool, int64_t rows, uint32_t bo
 
 using namespace ddt;
 
+namespace ddt {
+// Checks of a verify call that do not look at its pointers, in the order
+// ddtree_verify_attn applies them: sizes, then the device; on success
+// *workspace_bytes is the scratch the call needs (0 for an empty batch).
+int verify_precheck(const ddt_dims* dims, size_t* workspace_bytes) {
+  int rc = check_dims(dims);
+  if (rc != DDT_OK) return rc;
+  *workspace_bytes = 0;
+  if (dims->batch == 0) return DDT_OK;
+  DeviceInfo dev;
+  if ((rc = device_info(&dev)) != DDT_OK) return rc;
+  Plan plan;
+  if ((rc = make_plan(dims, dev.sm_count, &plan)) != DDT_OK) return rc;
+  *workspace_bytes = plan.bytes;
+  return DDT_OK;
+}
+}  // namespace ddt
+
 extern "C" size_t ddtree_verify_workspace_bytes(const ddt_dims* dims) {
   DeviceInfo dev;
   if (device_info(&dev) != DDT_OK) return 0;
@@ -188,9 +209,12 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
   float* o_part = reinterpret_cast<float*>(ws + plan.o_off);
 
   if (phases & kPhasePrefix) {
-    if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
+    if (cudaMemsetAsync(status, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
     if (plan.splits > 0) {
       PrefixParams pp;
+#ifdef DDT_TEST_HOOKS
+      pp.test_drop_step = g_test_drop_step;
+#endif
       // the 64-row box maps (steps of consecutive slots) only when the pool has 64 rows
       pp.block_loads = dims->pool_slots >= kKeysPerTile ? 1 : 0;
       if (!encode_pool_map(&pp.tmap_rows, kv_pool, dims->pool_slots, 64, 1) ||
@@ -303,6 +327,56 @@ extern "C" int ddtree_kv_compact(const void* kv_src, void* kv_dst, const int32_t
   return DDT_OK;
 }
 
+extern "C" int ddtree_kv_compact_check(const int32_t* slot_idx, const int32_t* prefix_len, const int64_t* dst_start,
+                                       const int32_t* tree_slot_idx, const ddt_dims* dims, int32_t same_pool,
+                                       int64_t* bad_slot) {
+  int rc = check_dims(dims);
+  if (rc != DDT_OK) return rc;
+  if (bad_slot) *bad_slot = -1;
+  const int B = dims->batch;
+  if (B == 0) return DDT_OK;
+  if (!prefix_len || !dst_start || (!slot_idx && dims->max_prefix_len > 0)) return DDT_ERR_NULL;
+  auto fail = [&](int64_t slot) {
+    if (bad_slot) *bad_slot = slot;
+    return DDT_ERR_ALIAS;
+  };
+  // destination ranges: inside the pool and pairwise disjoint
+  std::vector<std::pair<int64_t, int64_t>> dst;  // [begin, end)
+  dst.reserve(B);
+  for (int b = 0; b < B; ++b) {
+    const int64_t L = prefix_len[b];
+    if (L < 0 || L > dims->max_prefix_len) return DDT_ERR_DIMS;
+    if (L == 0) continue;
+    const int64_t d0 = dst_start[b];
+    if (d0 < 0 || d0 + L > dims->pool_slots) return fail(d0 < 0 ? d0 : d0 + L - 1);
+    dst.emplace_back(d0, d0 + L);
+  }
+  std::sort(dst.begin(), dst.end());
+  for (size_t i = 1; i < dst.size(); ++i)
+    if (dst[i].first < dst[i - 1].second) return fail(dst[i].first);
+  if (!same_pool) return DDT_OK;
+  // in place: no destination row may hold a live row that the copy (or a later
+  // verify call) still reads, except a row that is already where it goes
+  auto dst_hit = [&](int64_t slot) {
+    auto it = std::upper_bound(dst.begin(), dst.end(), std::make_pair(slot, INT64_MAX));
+    return it != dst.begin() && slot < std::prev(it)->second;
+  };
+  for (int b = 0; b < B; ++b) {
+    const int32_t* row = slot_idx + static_cast<int64_t>(b) * dims->slot_stride;
+    for (int32_t j = 0; j < prefix_len[b]; ++j) {
+      const int64_t src = row[j];
+      if (src == dst_start[b] + j) continue;  // already in place: the copy rewrites it with itself
+      if (dst_hit(src)) return fail(src);
+    }
+    if (tree_slot_idx)
+      for (int32_t u = 0; u < dims->num_nodes; ++u) {
+        const int64_t t = tree_slot_idx[static_cast<int64_t>(b) * dims->num_nodes + u];
+        if (dst_hit(t)) return fail(t);
+      }
+  }
+  return DDT_OK;
+}
+
 extern "C" int ddtree_read_device_status(const void* workspace, int32_t* host_status, ddt_stream_t stream) {
   if (!workspace || !host_status) return DDT_ERR_NULL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -311,6 +385,15 @@ extern "C" int ddtree_read_device_status(const void* workspace, int32_t* host_st
     return DDT_ERR_LAUNCH;
   return DDT_OK;
 }
+
+#ifdef DDT_TEST_HOOKS
+// Test builds only (not part of the public header): make the prefix kernel's
+// producers skip the loads of one step, so a bounded wait runs out.
+int32_t ddt::g_test_drop_step = -1;
+extern "C" __attribute__((visibility("default"))) void ddtree_test_set_drop_step(int32_t step) {
+  ddt::g_test_drop_step = step;
+}
+#endif
 
 extern "C" const char* ddtree_status_string(int code) {
   switch (code) {
@@ -321,6 +404,7 @@ extern "C" const char* ddtree_status_string(int code) {
     case DDT_ERR_ALIGN: return "a device pointer is misaligned";
     case DDT_ERR_LAUNCH: return "a kernel launch or CUDA runtime call failed";
     case DDT_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    case DDT_ERR_ALIAS: return "kv_compact destinations overlap each other or a live source row";
     default: return "unknown status";
   }
 }

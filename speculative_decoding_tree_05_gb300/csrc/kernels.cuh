@@ -41,7 +41,10 @@ struct PrefixParams {
   int32_t block_loads;       // tmap_block and tmap_rope are valid (pool has >= 64 rows)
   float* o_part;             // fp32 [B, max_splits, row_tiles*128, 512]
   float* lse_part;           // fp32 [B, max_splits, row_tiles*128], natural log
-  int32_t* status;
+  int32_t* status;           // status word; status[1] counts lazy O rescales in test builds
+#ifdef DDT_TEST_HOOKS
+  int32_t test_drop_step;    // test builds: producers load nothing for this step of every unit (-1: none)
+#endif
 };
 
 // Tree tail + merge: one CTA per (request, node, head group).
@@ -94,5 +97,11 @@ cudaError_t configure_tail_merge();
 cudaError_t launch_prefix(const PrefixParams& p, int batch, int splits, cudaStream_t stream);
 cudaError_t launch_tail_merge(const TailParams& p, int batch, cudaStream_t stream);
 cudaError_t launch_kv_compact(const CompactParams& p, int batch, cudaStream_t stream);
+
+#ifdef DDT_TEST_HOOKS
+// Test builds: the step whose stage loads the producers skip (-1: none), set by
+// ddtree_test_set_drop_step and copied into every prefix launch.
+extern int32_t g_test_drop_step;
+#endif
 
 }  // namespace ddt

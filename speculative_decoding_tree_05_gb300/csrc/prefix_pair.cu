@@ -27,13 +27,19 @@
 // other set's next step is ready to send, so one buffer costs no waiting.
 //
 // Partial-score exchange format: per row and 64-key step, block floating point
-// -- one power-of-two exponent e with every |x| < 2^e and 64 int16 mantissas
-// round(x * 2^(14-e)), x being the partial score in log2 units.  That is half
-// the bytes of fp32 (the exchange is bound by DSMEM bandwidth) with an error of
-// at most 2^-15 * 2^e, i.e. 2^-14 of the row's largest partial in the step.
-// Rounding to an integer and packing use the float adder: x * 2^(14-e) + M with
-// M = 1.5 * 2^23 + 2^15 is an integer-valued float whose low 16 bits are the
-// biased mantissa, so no int/float conversion instruction is needed.  Each CTA
+// -- one power-of-two exponent e with every |x| < 2^e and 64 20-bit mantissas
+// round(x * 2^(18-e)) + 2^19, x being the partial score in log2 units.  A
+// mantissa travels as its low 16 bits plus a 4-bit nibble (2.5 bytes instead of
+// fp32's 4: the exchange is bound by DSMEM bandwidth and the shared memory is
+// full).  The rounding error is at most 2^(e-19), i.e. 2^-18 of the row's
+// largest partial in the step; with partial scores below 2^9 log2 units
+// (355 nats) that is under 7e-4 nats, so the log-sum-exp stays within 1e-3 of
+// the exact one even for a dominant key.  (A 16-bit mantissa, error 2^(e-15),
+// already exceeds 1e-3 nats once partial scores reach 32 log2 units.)
+// Rounding to an integer and packing use the float adder: x * 2^(18-e) + M with
+// M = 1.5 * 2^23 + 2^19 is an integer-valued float whose low 20 bits are the
+// biased mantissa and whose high bits are 0x4B4, so no int/float conversion
+// instruction is needed either way.  Each CTA
 // adds the peer's decoded partial to its own unrounded one, so the two CTAs'
 // scores differ by that rounding alone; each CTA keeps its own running max and
 // row sum and normalises its own half of O by them, so neither half depends on
@@ -97,7 +103,10 @@ constexpr int kProducers = 96;
 constexpr int kSlotLookahead = 4;                        // producers fetch slot indices this many steps ahead
 constexpr int kGatherBlocks = 3;                         // latent blocks fetched by gather4 on scattered steps
 constexpr int kXSets = 2;                                // exchange barrier pairs (step t uses t % 2)
-constexpr int kXBytes = kTileRows * kNk * 2;             // 16384: int16 mantissas of one step
+constexpr int kXChunk = kTileRows * 16;                  // one 16-byte chunk of every row of the tile
+constexpr int kXLoChunks = kNk * 2 / 16;                 // 8: low 16 bits of the 64 mantissas
+constexpr int kXNibChunks = kNk / 2 / 16;                // 2: their top 4 bits, two per byte
+constexpr int kXBytes = (kXLoChunks + kXNibChunks) * kXChunk;  // 20480: 20-bit mantissas of one step
 constexpr int kEBytes = kTileRows * 4;                   // 512: one exponent per row
 constexpr int kQRopeBytes = kTileRows * 64;              // 8192: Q_r rope dims, 64-byte swizzle
 constexpr int kQLatSmemBytes = kTileRows * 128;          // 16384: Q_r latent dims 192..255, 128-byte swizzle
@@ -107,16 +116,20 @@ constexpr int kOffE = kOffX + kXBytes;
 constexpr int kOffQRope = kOffE + kEBytes;               // 512-byte aligned (64-byte swizzle atoms)
 static_assert(kOffQLat % 1024 == 0 && kOffQRope % 512 == 0, "swizzled operands need aligned bases");
 constexpr int kOffHand = kOffQRope + kQRopeBytes;        // [2][128] running max handed between sets
-constexpr int kOffFin = kOffHand + 2 * kTileRows * 4;    // [2 sets][2 (l, m)][128] final row state
-constexpr int kSmem = kOffFin + 2 * 2 * kTileRows * 4 + 1024;
+// [2 sets][2 (l, m)][128] final row state: written after the last exchange has
+// been read out, so it shares the exchange buffer
+constexpr int kOffFin = kOffX;
+static_assert(2 * 2 * kTileRows * 4 <= kXBytes, "the final row state fits in the exchange buffer");
+constexpr int kSmem = kOffHand + 2 * kTileRows * 4 + 1024;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 384, kColQ = 416, kTmemCols = 512;
 constexpr int kQTmemKSteps = 12;                         // Q_r latent dims 0..191 from TMEM, 192..255 from smem
 constexpr uint32_t kIdescS = idesc_bf16_f32(kTileRows, kNk, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileRows, 256, false, true);
 constexpr float kRescaleThreshold = 8.f;                 // log2 units
 constexpr float kLn2 = 0.69314718055994531f;
-constexpr float kMagic = 12615680.0f;                    // 1.5 * 2^23 + 2^15
-constexpr uint32_t kMagicHi = 0x4B400000u;               // bits of 1.5 * 2^23
+constexpr int kXFracBits = 18;                           // mantissa = round(x * 2^(18-e)) + 2^19, 20 bits
+constexpr float kMagic = 13107200.0f;                    // 1.5 * 2^23 + 2^19
+constexpr uint32_t kMagicHi = 0x4B4B4B4Bu;               // top byte of every encoded float, repeated
 constexpr int kSoftmaxBarrier = 1;                       // named barrier of the 256 softmax threads
 static_assert(kNk == 64, "the step layout assumes 64 keys");
 
@@ -288,7 +301,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       }
       // nothing of this thread's may still be running when TMEM is released (also after a timeout)
       mma_commit(&sh.mma_drain);
-      mbar_wait(&sh.mma_drain, 0, 1u << 20);
+      mbar_wait(&sh.mma_drain, 0);
     }
     __syncwarp();
     cluster_wait();
@@ -314,6 +327,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       pf[2 * kSlotLookahead - 2] = fetch(j + kSlotLookahead, 0);
       pf[2 * kSlotLookahead - 1] = fetch(j + kSlotLookahead, 1);
       const int st = j % kStages;
+#ifdef DDT_TEST_HOOKS
+      // test builds: a stage that is never loaded, so the waits for it run out
+      if (j == p.test_drop_step) continue;
+#endif
       // warp-uniform wait: the lane shuffles below need every lane
       const bool waited = j < kStages || mbar_wait_abortable(&sh.k_empty[st], ((j / kStages) - 1) & 1, abort);
       if (!__all_sync(0xffffffffu, waited)) {
@@ -466,7 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
       const float sl2 = p.scale_log2;
       const int e = block_exponent(amax * sl2);
-      const float enc = sl2 * pow2i(14 - e);
+      const float enc = sl2 * pow2i(kXFracBits - e);
       const uint64_t enc2 = f32x2(enc, enc), magic2 = f32x2(kMagic, kMagic);
       // the peer must have read step j-1 (the other set's) out of the buffer before it is overwritten
       if (j >= 1 && !__all_sync(0xffffffffu,
@@ -475,19 +492,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         break;
       }
       {
-        // chunk-major buffer [8 chunks][128 rows][16 B]: a warp's store of one chunk is 512 contiguous bytes
+        // chunk-major buffer [10 chunks][128 rows][16 B]: a warp's store of one chunk is 512 contiguous
+        // bytes.  Chunk c < 8 holds the low 16 bits of mantissas 8c..8c+7; chunk 8 + c/4, word c%4,
+        // their top nibbles (byte i: mantissa 8c+i in the low nibble, 8c+i+4 in the high one).
         const uint32_t xr = x_remote + r * 16, br = xbar_remote[xb_i];
+        uint32_t nib[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
+        for (int c = 0; c < kXLoChunks; ++c) {
+          uint32_t tb[8], w[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int k = 8 * c + 2 * q;
             float t0, t1;
             f32x2_split(fma_x2(f32x2(x[k], x[k + 1]), enc2, magic2), t0, t1);
-            w[q] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
+            tb[2 * q] = __float_as_uint(t0);
+            tb[2 * q + 1] = __float_as_uint(t1);
+            w[q] = __byte_perm(tb[2 * q], tb[2 * q + 1], 0x5410);
           }
-          st_async_v4(xr + c * (kTileRows * 16), make_uint4(w[0], w[1], w[2], w[3]), br);
+          st_async_v4(xr + c * kXChunk, make_uint4(w[0], w[1], w[2], w[3]), br);
+          // bits 16..19 sit in byte 2 of each encoded float (as 0x40 | nibble)
+          const uint32_t lo4 = __byte_perm(__byte_perm(tb[0], tb[1], 0x0062), __byte_perm(tb[2], tb[3], 0x6200), 0x7610);
+          const uint32_t hi4 = __byte_perm(__byte_perm(tb[4], tb[5], 0x0062), __byte_perm(tb[6], tb[7], 0x6200), 0x7610);
+          nib[c & 3] = (lo4 & 0x0F0F0F0Fu) | ((hi4 << 4) & 0xF0F0F0F0u);
+          if ((c & 3) == 3)
+            st_async_v4(xr + (kXLoChunks + (c >> 2)) * kXChunk, make_uint4(nib[0], nib[1], nib[2], nib[3]), br);
         }
         st_async_b32(e_remote + r * 4, static_cast<uint32_t>(e), br);
       }
@@ -505,17 +533,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       {
         const uint8_t* xbp = smem + kOffX + r * 16;
         const int pe = *reinterpret_cast<const int*>(smem + kOffE + r * 4);
-        const float pdec = pow2i(pe - 14), pm = -kMagic * pdec;
+        const float pdec = pow2i(pe - kXFracBits), pm = -kMagic * pdec;
         const uint64_t pdec2 = f32x2(pdec, pdec), pm2 = f32x2(pm, pm), sl22 = f32x2(sl2, sl2);
+        uint4 nv = *reinterpret_cast<const uint4*>(xbp + kXLoChunks * kXChunk);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xbp + c * (kTileRows * 16));
+        for (int c = 0; c < kXLoChunks; ++c) {
+          if (c == 4) nv = *reinterpret_cast<const uint4*>(xbp + (kXLoChunks + 1) * kXChunk);
+          const uint4 v = *reinterpret_cast<const uint4*>(xbp + c * kXChunk);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          const uint32_t nb = (c & 3) == 0 ? nv.x : (c & 3) == 1 ? nv.y : (c & 3) == 2 ? nv.z : nv.w;
+          const uint32_t nh = nb >> 4;
+          // byte 2 and 3 of each float: 0x40 | nibble, 0x4B (two mantissas per word)
+          const uint32_t hb[4] = {(__byte_perm(nb, kMagicHi, 0x4140) & 0xFF0FFF0Fu) | 0x00400040u,
+                                  (__byte_perm(nb, kMagicHi, 0x4342) & 0xFF0FFF0Fu) | 0x00400040u,
+                                  (__byte_perm(nh, kMagicHi, 0x4140) & 0xFF0FFF0Fu) | 0x00400040u,
+                                  (__byte_perm(nh, kMagicHi, 0x4342) & 0xFF0FFF0Fu) | 0x00400040u};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int k = 8 * c + 2 * q;
-            const uint64_t peer = fma_x2(f32x2(__uint_as_float(__byte_perm(w[q], kMagicHi, 0x7610)),
-                                               __uint_as_float(__byte_perm(w[q], kMagicHi, 0x7632))),
+            const uint64_t peer = fma_x2(f32x2(__uint_as_float(__byte_perm(w[q], hb[q], 0x5410)),
+                                               __uint_as_float(__byte_perm(w[q], hb[q], 0x7632))),
                                          pdec2, pm2);
             f32x2_split(fma_x2(f32x2(x[k], x[k + 1]), sl22, peer), x[k], x[k + 1]);
           }
@@ -546,6 +583,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       mbar_arrive(&sh.m_ready[sb]);
       const float alpha = (m_used == m_prev) ? 1.f : fast_exp2(m_prev - m_used);  // 0 on the first growth
       if (__any_sync(0xffffffffu, alpha != 1.f) && j > 0) {
+#ifdef DDT_TEST_HOOKS
+        if (lane == 0) atomicAdd(p.status + 1, 1);  // test builds count the lazy O rescales
+#endif
         // O must hold every earlier step: wait for P.V of step j-1 (MMAs complete in order)
         if (!__all_sync(0xffffffffu,
                         mbar_wait_abortable(&sh.k_empty[(j - 1) % kStages], ((j - 1) / kStages) & 1, abort))) {
@@ -603,7 +643,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       if (lead) {
         pv_ok = mbar_wait_abortable(&sh.p_ready[sb], (j / 2) & 1, abort);
         for (uint32_t spin = 0; pv_ok && sh.pv_next != j; ++spin)
-          if (spin > (1u << 24) || ((spin & 255) == 255 && *abort)) pv_ok = false;
+          if (spin > 4 * DDT_WAIT_LIMIT || ((spin & 255) == 255 && *abort)) pv_ok = false;
         if (pv_ok) {
           tc_fence_after();
           const uint64_t dv = desc_advance(d_v, (j % kStages) * kStageBytes);
@@ -623,9 +663,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 
     // epilogue: combine both sets' row sums, wait for the last P.V, then
     // o = O / l (set s writes O columns [128 s, 128 s + 128)) and lse.
+    // The row state shares the exchange buffer: write it only once both sets
+    // are past their last exchange (the other set may still be receiving one).
+    if (bar_red_or(kSoftmaxBarrier, 256, !ok)) ok = false;
     fin[(set * 2 + 0) * kTileRows + r] = l;
     fin[(set * 2 + 1) * kTileRows + r] = m_ref;
-    if (bar_red_or(kSoftmaxBarrier, 256, !ok)) ok = false;
+    bar_sync(kSoftmaxBarrier, 256);
     const float l_o = fin[((set ^ 1) * 2 + 0) * kTileRows + r], m_o = fin[((set ^ 1) * 2 + 1) * kTileRows + r];
     const float m_fin = fmaxf(m_ref, m_o);
     const float lrow = (l > 0.f ? l * fast_exp2(m_ref - m_fin) : 0.f) + (l_o > 0.f ? l_o * fast_exp2(m_o - m_fin) : 0.f);
@@ -668,7 +711,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
   if (warp >= 4 && (warp & 3) == 0 && lane == 0) {
     // the P.V MMAs this thread issued: all complete before TMEM is released (also after a timeout)
     mma_commit(&sh.mma_drain);
-    mbar_wait(&sh.mma_drain, 0, 1u << 20);
+    mbar_wait(&sh.mma_drain, 0);
   }
   if (!ok) {
     *abort = 1;
@@ -679,7 +722,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
   if (*abort && warp >= 1 && warp < 4 && lane == 0) {
     // after a timeout, bulk copies of unconsumed stages may still be landing:
     // wait for them (bounded) before the shared memory is released
-    for (int t = max(0, issued - kStages); t < issued; ++t) mbar_wait(&sh.k_full[t % kStages], (t / kStages) & 1, 1u << 20);
+    for (int t = max(0, issued - kStages); t < issued; ++t) mbar_wait(&sh.k_full[t % kStages], (t / kStages) & 1);
   }
   cluster_sync();  // no CTA leaves while its peer may still write into its shared memory
   if (warp == 0) {

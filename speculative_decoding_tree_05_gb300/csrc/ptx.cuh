@@ -2,6 +2,17 @@
 #pragma once
 #include <cstdint>
 
+// Iteration limits of the bounded on-chip waits (each mbarrier.try_wait itself
+// blocks for a while before it reports "not yet").  A wait that reaches its
+// limit gives up and the kernel reports DDT_STATUS_TIMEOUT.  Test builds
+// compile small limits in so that a test can make a wait run out quickly.
+#ifndef DDT_WAIT_LIMIT
+#define DDT_WAIT_LIMIT (1u << 22)
+#endif
+#ifndef DDT_DRAIN_LIMIT
+#define DDT_DRAIN_LIMIT (1u << 20)
+#endif
+
 namespace ddt {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -52,7 +63,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on the phase with the given parity.  Returns false when the
 // iteration limit is reached (each try_wait itself blocks for a while), so no
 // caller can spin forever.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 24)) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = DDT_DRAIN_LIMIT) {
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
@@ -77,7 +88,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 // Bounded waits that also give up as soon as another thread of the CTA has
 // raised *abort (a volatile shared flag), so one expired wait ends them all.
 __device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                    bool cluster_scope = false, uint32_t limit = (1u << 22)) {
+                                                    bool cluster_scope = false, uint32_t limit = DDT_WAIT_LIMIT) {
   for (uint32_t i = 0; i < limit; ++i) {
     if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 63 && *abort) return false;
@@ -97,6 +108,11 @@ __device__ __forceinline__ bool bar_red_or(int id, int count, bool pred) {
       : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
       : "memory");
   return r != 0;
+}
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- clusters / DSMEM

@@ -16,6 +16,7 @@
 #include "../../include/ddtree.h"
 
 namespace ddt {
+int verify_precheck(const ddt_dims* dims, size_t* workspace_bytes);  // api.cu
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;
@@ -50,13 +51,13 @@ extern "C" int ddtree_verify_attn_static_scratch(const void* q, const void* kv_p
                                                  const int32_t* prefix_len, const int32_t* tree_parent,
                                                  const int32_t* tree_slot_idx, float sm_scale, float* out,
                                                  float* lse, const ddt_dims* dims, ddt_stream_t stream) {
-  if (!dims) return DDT_ERR_NULL;
+  size_t need = 0;
+  int rc = ddt::verify_precheck(dims, &need);  // the size and device checks of ddtree_verify_attn, same codes
+  if (rc != DDT_OK) return rc;
   if (dims->batch == 0) return DDT_OK;
-  const size_t need = ddtree_verify_workspace_bytes(dims);
-  if (need == 0) return DDT_ERR_DIMS;
   if (need > ddt::kStaticScratchBytes) return DDT_ERR_WORKSPACE;
   void* scratch = nullptr;
-  const int rc = ddt::static_scratch(&scratch);
+  rc = ddt::static_scratch(&scratch);
   if (rc != DDT_OK) return rc;
   return ddtree_verify_attn(q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out, lse, dims,
                             scratch, ddt::kStaticScratchBytes, stream);

@@ -17,7 +17,7 @@ D_V = 512
 
 DDT_OK = 0
 ERRORS = {-1: "DDT_ERR_NULL", -2: "DDT_ERR_DIMS", -3: "DDT_ERR_WORKSPACE", -4: "DDT_ERR_ALIGN",
-          -5: "DDT_ERR_LAUNCH", -6: "DDT_ERR_DEVICE"}
+          -5: "DDT_ERR_LAUNCH", -6: "DDT_ERR_DEVICE", -7: "DDT_ERR_ALIAS"}
 STATUS_BAD_SLOT = 1
 STATUS_BAD_PARENT = 2
 STATUS_BAD_PREFIX = 4
@@ -27,6 +27,7 @@ STATUS_BAD_TREE_LEN = 16
 EXPORTS = ("ddtree_verify_workspace_bytes", "ddtree_verify_attn", "ddtree_verify_attn_ragged",
            "ddtree_verify_prefix_phase",
            "ddtree_verify_merge_phase", "ddtree_verify_attn_static_scratch", "ddtree_kv_compact",
+           "ddtree_kv_compact_check",
            "ddtree_read_device_status", "ddtree_status_string")
 
 
@@ -45,34 +46,45 @@ class Dims(ctypes.Structure):
 _lib = None
 
 
+def load(path: str):
+    """Load a build of the library from `path` and declare its C signatures.
+
+    lib() loads the product build; tests also load the test-hooks build this way.
+    """
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing (run __graft_entry__.build())")
+    L = ctypes.CDLL(path)
+    vp, i32p = ctypes.c_void_p, ctypes.c_void_p
+    L.ddtree_verify_workspace_bytes.restype = ctypes.c_size_t
+    L.ddtree_verify_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+    for fn in ("ddtree_verify_attn", "ddtree_verify_prefix_phase", "ddtree_verify_merge_phase"):
+        f = getattr(L, fn)
+        f.restype = ctypes.c_int
+        f.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp, ctypes.POINTER(Dims), vp,
+                      ctypes.c_size_t, vp]
+    L.ddtree_verify_attn_ragged.restype = ctypes.c_int
+    L.ddtree_verify_attn_ragged.argtypes = [vp, vp, i32p, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp,
+                                            ctypes.POINTER(Dims), vp, ctypes.c_size_t, vp]
+    L.ddtree_verify_attn_static_scratch.restype = ctypes.c_int
+    L.ddtree_verify_attn_static_scratch.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp,
+                                                    ctypes.POINTER(Dims), vp]
+    L.ddtree_kv_compact.restype = ctypes.c_int
+    L.ddtree_kv_compact.argtypes = [vp, vp, i32p, i32p, vp, i32p, ctypes.POINTER(Dims), vp, vp]
+    L.ddtree_kv_compact_check.restype = ctypes.c_int
+    L.ddtree_kv_compact_check.argtypes = [vp, vp, vp, vp, ctypes.POINTER(Dims), ctypes.c_int32,
+                                          ctypes.POINTER(ctypes.c_int64)]
+    L.ddtree_read_device_status.restype = ctypes.c_int
+    L.ddtree_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+    L.ddtree_status_string.restype = ctypes.c_char_p
+    L.ddtree_status_string.argtypes = [ctypes.c_int]
+    return L
+
+
 def lib():
     """Load lib/libddtree.so (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing (run __graft_entry__.build())")
-        L = ctypes.CDLL(LIB_PATH)
-        vp, i32p = ctypes.c_void_p, ctypes.c_void_p
-        L.ddtree_verify_workspace_bytes.restype = ctypes.c_size_t
-        L.ddtree_verify_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
-        for fn in ("ddtree_verify_attn", "ddtree_verify_prefix_phase", "ddtree_verify_merge_phase"):
-            f = getattr(L, fn)
-            f.restype = ctypes.c_int
-            f.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp, ctypes.POINTER(Dims), vp,
-                          ctypes.c_size_t, vp]
-        L.ddtree_verify_attn_ragged.restype = ctypes.c_int
-        L.ddtree_verify_attn_ragged.argtypes = [vp, vp, i32p, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp,
-                                                ctypes.POINTER(Dims), vp, ctypes.c_size_t, vp]
-        L.ddtree_verify_attn_static_scratch.restype = ctypes.c_int
-        L.ddtree_verify_attn_static_scratch.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp,
-                                                        ctypes.POINTER(Dims), vp]
-        L.ddtree_kv_compact.restype = ctypes.c_int
-        L.ddtree_kv_compact.argtypes = [vp, vp, i32p, i32p, vp, i32p, ctypes.POINTER(Dims), vp, vp]
-        L.ddtree_read_device_status.restype = ctypes.c_int
-        L.ddtree_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
-        L.ddtree_status_string.restype = ctypes.c_char_p
-        L.ddtree_status_string.argtypes = [ctypes.c_int]
-        _lib = L
+        _lib = load(LIB_PATH)
     return _lib
 
 
@@ -113,13 +125,14 @@ class Verifier:
     """
 
     def __init__(self, batch, nodes, heads, pool_slots, slot_stride, max_prefix_len=None, device=None,
-                 prefix_len_sum=0):
+                 prefix_len_sum=0, library=None):
         import torch
+        self.lib = lib() if library is None else library
         self.dims = make_dims(batch, nodes, heads, pool_slots, slot_stride,
                               slot_stride if max_prefix_len is None else max_prefix_len, prefix_len_sum)
         self.device = torch.device("cuda") if device is None else torch.device(device)
         with torch.cuda.device(self.device):
-            n = workspace_bytes(self.dims)
+            n = int(self.lib.ddtree_verify_workspace_bytes(ctypes.byref(self.dims)))
             if n == 0:
                 raise DDTError(-2, "ddtree_verify_workspace_bytes")
             self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device)
@@ -140,7 +153,7 @@ class Verifier:
         if tree_len is not None:
             if phase != "all":
                 raise ValueError("ragged trees run as one call (phase='all')")
-            rc = lib().ddtree_verify_attn_ragged(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len),
+            rc = self.lib.ddtree_verify_attn_ragged(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len),
                                                  _ptr(tree_parent), _ptr(tree_slot_idx), _ptr(tree_len),
                                                  float(sm_scale), _ptr(out), _ptr(lse), ctypes.byref(self.dims),
                                                  _ptr(self.workspace), self.workspace.numel(), _stream(stream))
@@ -148,7 +161,7 @@ class Verifier:
             return out, lse
         fn = {"all": "ddtree_verify_attn", "prefix": "ddtree_verify_prefix_phase",
               "merge": "ddtree_verify_merge_phase"}[phase]
-        rc = getattr(lib(), fn)(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len), _ptr(tree_parent),
+        rc = getattr(self.lib, fn)(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len), _ptr(tree_parent),
                                 _ptr(tree_slot_idx), float(sm_scale), _ptr(out), _ptr(lse),
                                 ctypes.byref(self.dims), _ptr(self.workspace), self.workspace.numel(),
                                 _stream(stream))
@@ -156,7 +169,7 @@ class Verifier:
         return out, lse
 
     def status(self, stream=None) -> int:
-        return read_device_status(self.workspace, stream)
+        return read_device_status(self.workspace, stream, library=self.lib)
 
 
 def verify_attn(q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, max_prefix_len=None,
@@ -184,11 +197,47 @@ def verify_attn_static_scratch(q, kv_pool, slot_idx, prefix_len, tree_parent, tr
     return out, lse
 
 
+def kv_compact_check(slot_idx, prefix_len, dst_start, pool_slots, same_pool=True, tree_slot_idx=None,
+                     max_prefix_len=None):
+    """Host-side check of kv_compact's aliasing contract (numpy arrays or CPU tensors).
+
+    Returns (code, first offending slot or -1); code is DDT_OK or DDT_ERR_ALIAS (-7).
+    """
+    import numpy as np
+    si = np.ascontiguousarray(np.asarray(slot_idx), dtype=np.int32)
+    pl = np.ascontiguousarray(np.asarray(prefix_len), dtype=np.int32)
+    ds = np.ascontiguousarray(np.asarray(dst_start), dtype=np.int64)
+    B, stride = si.shape
+    T = 1
+    ts = None
+    if tree_slot_idx is not None:
+        ts = np.ascontiguousarray(np.asarray(tree_slot_idx), dtype=np.int32)
+        T = ts.shape[1]
+    dims = make_dims(B, T, 1, pool_slots, stride, stride if max_prefix_len is None else max_prefix_len)
+    bad = ctypes.c_int64(-1)
+    p = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    rc = lib().ddtree_kv_compact_check(p(si), p(pl), p(ds), p(ts), ctypes.byref(dims), int(bool(same_pool)),
+                                       ctypes.byref(bad))
+    return int(rc), int(bad.value)
+
+
 def kv_compact(kv_src, kv_dst, slot_idx, prefix_len, dst_start, slot_idx_out=None, max_prefix_len=None,
-               workspace=None, stream=None):
-    """Copy each request's prefix rows to dst_start[b] + j; returns slot_idx_out."""
+               workspace=None, stream=None, validate=False, tree_slot_idx=None):
+    """Copy each request's prefix rows to dst_start[b] + j; returns slot_idx_out.
+
+    validate=True first runs kv_compact_check on host copies of the tables (a
+    debug option: it synchronises with the device) and raises DDTError if the
+    aliasing contract is broken.
+    """
     import torch
     B, stride = slot_idx.shape
+    if validate:
+        rc, bad = kv_compact_check(slot_idx.cpu().numpy(), prefix_len.cpu().numpy(), dst_start.cpu().numpy(),
+                                   kv_src.shape[0], same_pool=kv_src.data_ptr() == kv_dst.data_ptr(),
+                                   tree_slot_idx=None if tree_slot_idx is None else tree_slot_idx.cpu().numpy(),
+                                   max_prefix_len=max_prefix_len)
+        if rc != DDT_OK:
+            raise DDTError(rc, f"kv_compact_check (slot {bad})")
     if slot_idx_out is None:
         slot_idx_out = slot_idx.clone()
     if workspace is None:
@@ -200,8 +249,8 @@ def kv_compact(kv_src, kv_dst, slot_idx, prefix_len, dst_start, slot_idx_out=Non
     return slot_idx_out
 
 
-def read_device_status(workspace, stream=None) -> int:
+def read_device_status(workspace, stream=None, library=None) -> int:
     st = ctypes.c_int32(0)
-    rc = lib().ddtree_read_device_status(_ptr(workspace), ctypes.byref(st), _stream(stream))
+    rc = (lib() if library is None else library).ddtree_read_device_status(_ptr(workspace), ctypes.byref(st), _stream(stream))
     _check(rc, "ddtree_read_device_status")
     return int(st.value)

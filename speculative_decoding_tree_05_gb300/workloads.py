@@ -40,7 +40,7 @@ class Config:
     batch: int
     prefix: tuple            # (L,) for every request, ("uniform", lo, hi) or ("list", L0, L1, ...)
     nodes: int               # tree nodes per request (node 0 is the root)
-    tree: str                # "random" or "chain"
+    tree: str                # "random", "chain" or "star"
     max_depth: int
     max_branch: int          # 0 = no cap on children per node
     heads: int
@@ -119,6 +119,13 @@ def random_tree(rng: np.random.Generator, nodes: int, max_depth: int, max_branch
 
 def chain_tree(nodes: int) -> np.ndarray:
     return np.arange(-1, nodes - 1, dtype=np.int32)
+
+
+def star_tree(nodes: int) -> np.ndarray:
+    """Root plus nodes-1 children of the root."""
+    p = np.zeros(nodes, dtype=np.int32)
+    p[0] = -1
+    return p
 
 
 def tree_depths(parent: np.ndarray) -> np.ndarray:
@@ -305,6 +312,8 @@ def make_workload(name: str, seed: int | None = None, slots: str | None = None,
     prefix_len = _prefix_lengths(cfg, s_struct)
     if cfg.tree == "chain":
         parents = np.stack([chain_tree(T) for _ in range(B)])
+    elif cfg.tree == "star":
+        parents = np.stack([star_tree(T) for _ in range(B)])
     else:
         parents = np.stack([random_tree(s_struct, T, cfg.max_depth, cfg.max_branch) for _ in range(B)])
 
@@ -368,3 +377,68 @@ def to_device(w: Workload, device="cuda", poison: bool = True):
         "tree_parent": t(w.tree_parent),
         "tree_slot_idx": t(w.tree_slot_idx),
     }
+
+
+# ----------------------------------------------------------------------------- closed cases
+
+def pow2_scaled_bits(bits: np.ndarray, k: int) -> np.ndarray:
+    """bf16 values times 2^k (exact for normal values that stay in range); returns bf16 bits."""
+    f = bf16_bits_to_f32(bits) * np.float32(2.0 ** k)
+    if not np.isfinite(f).all():
+        raise ValueError("scaling overflows bf16")
+    return f32_to_bf16_bits(f)
+
+
+CLOSED_CASES = {
+    # name: (make_workload overrides, value pattern)
+    "decode": (dict(prefix=(3000,), nodes=1, heads=16, tree="chain"), None),
+    "chain": (dict(prefix=(2000,), nodes=65, heads=16, tree="chain"), None),
+    "star": (dict(prefix=(2000,), nodes=33, heads=16, tree="star"), None),
+    "identical_keys": (dict(prefix=(5000,), nodes=9, heads=16), "identical"),
+    "dominant_key": (dict(prefix=(3000,), nodes=9, heads=16), "dominant"),
+    "tree_only_deep": (dict(prefix=(0,), nodes=128, heads=4, tree="chain"), None),
+    "q_x4": (dict(prefix=(8192,), nodes=65, heads=16, max_depth=8, max_branch=4), "q4"),
+    "q_x8": (dict(prefix=(8192,), nodes=65, heads=16, max_depth=8, max_branch=4), "q8"),
+    "growing_scores": (dict(prefix=(8192,), nodes=17, heads=16, max_depth=4, max_branch=4), "growing"),
+}
+
+
+def closed_case(kind: str, seed: int = 0xDD7EC000) -> Workload:
+    """Inputs of the method's closed and edge cases, seeded; small pool with churned slots.
+
+    identical  every prefix row is the same latent row
+    dominant   each query row is 4x one prefix key row (chosen per row): that key's
+               score exceeds the others by ~160 nats
+    q4, q8     queries scaled by 4 or 8 (partial scores of tens of log2 units)
+    growing    keys drift along one direction that every query shares, so scores
+               grow by ~2 nats per 64 keys (~250 over 8192 keys) and the running max of the online
+               softmax keeps rising across the steps of a key split
+    """
+    overrides, pattern = CLOSED_CASES[kind]
+    kw = dict(max_depth=8, max_branch=0, pool_slots=1 << 16, slots="churn")
+    kw.update(overrides)
+    w = make_workload("tiny", seed=seed, **kw)
+    rng = np.random.Generator(np.random.PCG64(seed + 1))
+    if pattern == "identical":
+        w.kv_prefix_bits = [np.broadcast_to(kp[:1], kp.shape).copy() for kp in w.kv_prefix_bits]
+    elif pattern == "dominant":
+        q = w.q_bits.copy()
+        for b in range(w.batch):
+            L = int(w.prefix_len[b])
+            pick = rng.integers(0, L, size=(w.nodes, w.heads))
+            q[b] = pow2_scaled_bits(w.kv_prefix_bits[b][pick], 2)
+        w.q_bits = q
+    elif pattern in ("q4", "q8"):
+        w.q_bits = pow2_scaled_bits(w.q_bits, 2 if pattern == "q4" else 3)
+    elif pattern == "growing":
+        u = rng.standard_normal(D_QK).astype(np.float32)
+        q = bf16_bits_to_f32(w.q_bits) * np.float32(0.25) + u
+        w.q_bits = f32_to_bf16_bits(q.astype(np.float32))
+        rows = []
+        for b in range(w.batch):
+            L = int(w.prefix_len[b])
+            ramp = (np.arange(L, dtype=np.float32) * np.float32(0.00075))[:, None]
+            rows.append(f32_to_bf16_bits(bf16_bits_to_f32(w.kv_prefix_bits[b]) + ramp * u[None, :]))
+        w.kv_prefix_bits = rows
+    w.name = f"closed:{kind}"
+    return w

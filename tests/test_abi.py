@@ -104,3 +104,21 @@ def test_ragged_host_checks(lib):
     assert ragged(ctypes.c_void_p(0x10002)) == -4   # misaligned int32 array
     assert ragged(None, dims(batch=0)) == 0         # empty batch: nothing enqueued
     assert ragged(p, dims(heads=0)) == -2
+
+
+def test_static_scratch_checks_sizes_first(lib):
+    # the same code as ddtree_verify_attn for unsupported sizes, before any device query
+    p = ctypes.c_void_p(0x10000)
+    bad = dims(nodes=0)
+    assert lib.ddtree_verify_attn_static_scratch(p, p, p, p, p, p, 0.1, p, p, ctypes.byref(bad), None) == -2
+    assert lib.ddtree_verify_attn_static_scratch(p, p, p, p, p, p, 0.1, p, p, None, None) == -1
+    assert lib.ddtree_verify_attn_static_scratch(p, p, p, p, p, p, 0.1, p, p, ctypes.byref(dims(batch=0)),
+                                                 None) == 0
+
+
+def test_static_scratch_without_sm103_is_a_device_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    p = ctypes.c_void_p(0x10000)
+    assert lib.ddtree_verify_attn_static_scratch(p, p, p, p, p, p, 0.1, p, p, ctypes.byref(dims()), None) == -6

@@ -85,3 +85,61 @@ def test_plan_compaction_moves_fragmented_requests_to_disjoint_runs():
     for b, L in enumerate(lens):
         if L and defrag.fragmentation(tables[b])["contiguous_steps"] < 1.0:
             assert b in moved
+
+
+# ----------------------------------------------------------------------------- kv_compact aliasing validator
+
+def _check(slot_idx, prefix_len, dst_start, pool=1000, same_pool=True, tree=None):
+    from speculative_decoding_tree_05_gb300 import build, ddtree
+    build.build()
+    return ddtree.kv_compact_check(np.asarray(slot_idx), np.asarray(prefix_len), np.asarray(dst_start), pool,
+                                   same_pool=same_pool, tree_slot_idx=tree)
+
+
+def test_compact_check_accepts_disjoint_plan():
+    assert _check([[5, 9, 7], [1, 2, 3]], [3, 3], [100, 200]) == (0, -1)
+
+
+def test_compact_check_rejects_destination_over_live_source():
+    # request 1's source slot 101 lies in request 0's destination [100, 103)
+    assert _check([[5, 9, 7], [101, 2, 3]], [3, 3], [100, 200]) == (-7, 101)
+
+
+def test_compact_check_allows_rows_already_in_place():
+    assert _check([[100, 101, 7]], [3], [100]) == (0, -1)
+
+
+def test_compact_check_rejects_overlapping_destinations():
+    assert _check([[5, 9, 7], [1, 2, 3]], [3, 3], [100, 102]) == (-7, 102)
+
+
+def test_compact_check_rejects_destination_outside_pool():
+    assert _check([[5, 9, 7]], [3], [998], pool=1000)[0] == -7
+
+
+def test_compact_check_two_pools_ignore_sources():
+    assert _check([[100, 9, 7]], [3], [99], same_pool=False) == (0, -1)
+    assert _check([[100, 9, 7]], [3], [99], same_pool=True) == (-7, 100)
+
+
+def test_compact_check_protects_tree_rows():
+    assert _check([[5, 9, 7]], [3], [100], tree=[[50, 102]]) == (-7, 102)
+    assert _check([[5, 9, 7]], [3], [100], tree=[[50, 103]]) == (0, -1)
+
+
+def test_compact_check_accepts_the_defrag_plan():
+    # the planner's in-place plan for a churned pool satisfies the contract
+    w = wl.make_workload("tiny", batch=3, prefix=("list", 700, 300, 900), nodes=9, heads=2, pool_slots=1 << 14,
+                         slots="churn")
+    used = w.used_slots()
+    free = np.setdiff1d(np.arange(1, w.pool_slots), used)
+    plan = defrag.plan_compaction(w.slot_idx, w.prefix_len, defrag.SortedFreeList(w.pool_slots, free))
+    assert len(plan.requests) > 0
+    r = plan.requests
+    rc, bad = _check(w.slot_idx[r], w.prefix_len[r], plan.dst_start, pool=w.pool_slots, tree=w.tree_slot_idx[r])
+    assert rc == 0, bad
+    # a plan that puts a request's destination over its own live rows (shifted by 3) is caught
+    bad_start = plan.dst_start.copy()
+    bad_start[0] = int(w.slot_idx[r[0], 5]) - 3
+    rc, bad = _check(w.slot_idx[r], w.prefix_len[r], bad_start, pool=w.pool_slots)
+    assert rc == -7
