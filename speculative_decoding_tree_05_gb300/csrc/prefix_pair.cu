@@ -27,18 +27,25 @@
 // other set's next step is ready to send, so one buffer costs no waiting.
 //
 // Partial-score exchange format: per row and 64-key step, block floating point
-// -- one power-of-two exponent e with every |x| < 2^e and 64 20-bit mantissas
-// round(x * 2^(18-e)) + 2^19, x being the partial score in log2 units.  A
-// mantissa travels as its low 16 bits plus a 4-bit nibble (2.5 bytes instead of
-// fp32's 4: the exchange is bound by DSMEM bandwidth and the shared memory is
-// full).  The rounding error is at most 2^(e-19), i.e. 2^-18 of the row's
-// largest partial in the step; with partial scores below 2^9 log2 units
-// (355 nats) that is under 7e-4 nats, so the log-sum-exp stays within 1e-3 of
-// the exact one even for a dominant key.  (A 16-bit mantissa, error 2^(e-15),
-// already exceeds 1e-3 nats once partial scores reach 32 log2 units.)
-// Rounding to an integer and packing use the float adder: x * 2^(18-e) + M with
-// M = 1.5 * 2^23 + 2^19 is an integer-valued float whose low 20 bits are the
-// biased mantissa and whose high bits are 0x4B4, so no int/float conversion
+// -- one power-of-two exponent e with every |x| < 2^e and 64 mantissas, x being
+// the partial score in log2 units.  Two widths, chosen per warp and step (the
+// receiving warp holds the same 32 rows, so it branches uniformly too):
+//   16-bit  round(x * 2^(14-e)) + 2^15, error <= 2^(e-15), used while every
+//           row of the warp has e <= 4 (error <= 2^-11 log2 units = 3.4e-4 nats;
+//           N(0,1) data at sm_scale 1/sqrt(192) stays there);
+//   20-bit  round(x * 2^(18-e)) + 2^19, error <= 2^(e-19): under 7e-4 nats for
+//           partial scores below 2^9 log2 units (355 nats).  A mantissa travels
+//           as its low 16 bits plus a 4-bit nibble.
+// Either way the log-sum-exp stays within 1e-3 of the exact one even for a
+// dominant key (a 16-bit mantissa alone exceeds 1e-3 nats once partial scores
+// reach 32 log2 units).  The buffer always carries 10 chunks per row (the two
+// nibble chunks are filler in 16-bit mode), so the byte count each receive
+// expects is fixed; the exponent word carries the width (bit 16).  That is at
+// most 2.5 bytes per score instead of fp32's 4: the exchange is bound by DSMEM
+// bandwidth and the shared memory is full.
+// Rounding to an integer and packing use the float adder: x * 2^(k-e) + M with
+// M = 1.5 * 2^23 + 2^(k+1) is an integer-valued float whose low k+2 bits are
+// the biased mantissa and whose high bits are fixed, so no int/float conversion
 // instruction is needed either way.  Each CTA
 // adds the peer's decoded partial to its own unrounded one, so the two CTAs'
 // scores differ by that rounding alone; each CTA keeps its own running max and
@@ -127,9 +134,14 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(kTileRows, kNk, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileRows, 256, false, true);
 constexpr float kRescaleThreshold = 8.f;                 // log2 units
 constexpr float kLn2 = 0.69314718055994531f;
-constexpr int kXFracBits = 18;                           // mantissa = round(x * 2^(18-e)) + 2^19, 20 bits
+constexpr int kXFracBits = 18;                           // 20-bit mantissa = round(x * 2^(18-e)) + 2^19
 constexpr float kMagic = 13107200.0f;                    // 1.5 * 2^23 + 2^19
 constexpr uint32_t kMagicHi = 0x4B4B4B4Bu;               // top byte of every encoded float, repeated
+constexpr int kXFracBits16 = 14;                         // 16-bit mantissa = round(x * 2^(14-e)) + 2^15
+constexpr float kMagic16 = 12615680.0f;                  // 1.5 * 2^23 + 2^15
+constexpr uint32_t kMagicHi16 = 0x4B400000u;             // top half of every 16-bit-encoded float
+constexpr int kX16MaxExp = 4;                            // 16-bit mantissas while every e of the warp is <= 4
+constexpr uint32_t kXWide = 1u << 16;                    // exponent word flag: 20-bit mantissas
 constexpr int kSoftmaxBarrier = 1;                       // named barrier of the 256 softmax threads
 static_assert(kNk == 64, "the step layout assumes 64 keys");
 
@@ -483,8 +495,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
       const float sl2 = p.scale_log2;
       const int e = block_exponent(amax * sl2);
-      const float enc = sl2 * pow2i(kXFracBits - e);
-      const uint64_t enc2 = f32x2(enc, enc), magic2 = f32x2(kMagic, kMagic);
+      const bool wide = __any_sync(0xffffffffu, e > kX16MaxExp);
+      const float enc = sl2 * pow2i((wide ? kXFracBits : kXFracBits16) - e);
+      const float magic = wide ? kMagic : kMagic16;
+      const uint64_t enc2 = f32x2(enc, enc), magic2 = f32x2(magic, magic);
       // the peer must have read step j-1 (the other set's) out of the buffer before it is overwritten
       if (j >= 1 && !__all_sync(0xffffffffu,
                                 mbar_wait_abortable(&sh.x_free[xb_i ^ 1], ((j - 1) / 2) & 1, abort, true))) {
@@ -493,10 +507,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       }
       {
         // chunk-major buffer [10 chunks][128 rows][16 B]: a warp's store of one chunk is 512 contiguous
-        // bytes.  Chunk c < 8 holds the low 16 bits of mantissas 8c..8c+7; chunk 8 + c/4, word c%4,
-        // their top nibbles (byte i: mantissa 8c+i in the low nibble, 8c+i+4 in the high one).
+        // bytes.  Chunk c < 8 holds the low 16 bits of mantissas 8c..8c+7; in 20-bit mode chunk 8 + c/4,
+        // word c%4, holds their top nibbles (byte i: mantissa 8c+i in the low nibble, 8c+i+4 in the high).
         const uint32_t xr = x_remote + r * 16, br = xbar_remote[xb_i];
-        uint32_t nib[4];
+        uint32_t nib[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int c = 0; c < kXLoChunks; ++c) {
           uint32_t tb[8], w[4];
@@ -510,14 +524,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
             w[q] = __byte_perm(tb[2 * q], tb[2 * q + 1], 0x5410);
           }
           st_async_v4(xr + c * kXChunk, make_uint4(w[0], w[1], w[2], w[3]), br);
-          // bits 16..19 sit in byte 2 of each encoded float (as 0x40 | nibble)
-          const uint32_t lo4 = __byte_perm(__byte_perm(tb[0], tb[1], 0x0062), __byte_perm(tb[2], tb[3], 0x6200), 0x7610);
-          const uint32_t hi4 = __byte_perm(__byte_perm(tb[4], tb[5], 0x0062), __byte_perm(tb[6], tb[7], 0x6200), 0x7610);
-          nib[c & 3] = (lo4 & 0x0F0F0F0Fu) | ((hi4 << 4) & 0xF0F0F0F0u);
+          if (wide) {
+            // bits 16..19 sit in byte 2 of each encoded float (as 0x40 | nibble)
+            const uint32_t lo4 = __byte_perm(__byte_perm(tb[0], tb[1], 0x0062), __byte_perm(tb[2], tb[3], 0x6200), 0x7610);
+            const uint32_t hi4 = __byte_perm(__byte_perm(tb[4], tb[5], 0x0062), __byte_perm(tb[6], tb[7], 0x6200), 0x7610);
+            nib[c & 3] = (lo4 & 0x0F0F0F0Fu) | ((hi4 << 4) & 0xF0F0F0F0u);
+          }
           if ((c & 3) == 3)
             st_async_v4(xr + (kXLoChunks + (c >> 2)) * kXChunk, make_uint4(nib[0], nib[1], nib[2], nib[3]), br);
         }
-        st_async_b32(e_remote + r * 4, static_cast<uint32_t>(e), br);
+        st_async_b32(e_remote + r * 4, (static_cast<uint32_t>(e) & 0xFFFFu) | (wide ? kXWide : 0u), br);
       }
       // key mask of this step (past the split end or a slot outside the pool)
       const uint32_t masked0 = __ballot_sync(
@@ -532,29 +548,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       float mx = -CUDART_INF_F;
       {
         const uint8_t* xbp = smem + kOffX + r * 16;
-        const int pe = *reinterpret_cast<const int*>(smem + kOffE + r * 4);
-        const float pdec = pow2i(pe - kXFracBits), pm = -kMagic * pdec;
-        const uint64_t pdec2 = f32x2(pdec, pdec), pm2 = f32x2(pm, pm), sl22 = f32x2(sl2, sl2);
-        uint4 nv = *reinterpret_cast<const uint4*>(xbp + kXLoChunks * kXChunk);
+        const uint32_t ew = *reinterpret_cast<const uint32_t*>(smem + kOffE + r * 4);
+        const int pe = static_cast<int16_t>(ew & 0xFFFFu);
+        const uint64_t sl22 = f32x2(sl2, sl2);
+        if (ew & kXWide) {
+          const float pdec = pow2i(pe - kXFracBits), pm = -kMagic * pdec;
+          const uint64_t pdec2 = f32x2(pdec, pdec), pm2 = f32x2(pm, pm);
+          uint4 nv = *reinterpret_cast<const uint4*>(xbp + kXLoChunks * kXChunk);
 #pragma unroll
-        for (int c = 0; c < kXLoChunks; ++c) {
-          if (c == 4) nv = *reinterpret_cast<const uint4*>(xbp + (kXLoChunks + 1) * kXChunk);
-          const uint4 v = *reinterpret_cast<const uint4*>(xbp + c * kXChunk);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          const uint32_t nb = (c & 3) == 0 ? nv.x : (c & 3) == 1 ? nv.y : (c & 3) == 2 ? nv.z : nv.w;
-          const uint32_t nh = nb >> 4;
-          // byte 2 and 3 of each float: 0x40 | nibble, 0x4B (two mantissas per word)
-          const uint32_t hb[4] = {(__byte_perm(nb, kMagicHi, 0x4140) & 0xFF0FFF0Fu) | 0x00400040u,
-                                  (__byte_perm(nb, kMagicHi, 0x4342) & 0xFF0FFF0Fu) | 0x00400040u,
-                                  (__byte_perm(nh, kMagicHi, 0x4140) & 0xFF0FFF0Fu) | 0x00400040u,
-                                  (__byte_perm(nh, kMagicHi, 0x4342) & 0xFF0FFF0Fu) | 0x00400040u};
+          for (int c = 0; c < kXLoChunks; ++c) {
+            if (c == 4) nv = *reinterpret_cast<const uint4*>(xbp + (kXLoChunks + 1) * kXChunk);
+            const uint4 v = *reinterpret_cast<const uint4*>(xbp + c * kXChunk);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            const uint32_t nb = (c & 3) == 0 ? nv.x : (c & 3) == 1 ? nv.y : (c & 3) == 2 ? nv.z : nv.w;
+            const uint32_t nh = nb >> 4;
+            // byte 2 and 3 of each float: 0x40 | nibble, 0x4B (two mantissas per word)
+            const uint32_t hb[4] = {(__byte_perm(nb, kMagicHi, 0x4140) & 0xFF0FFF0Fu) | 0x00400040u,
+                                    (__byte_perm(nb, kMagicHi, 0x4342) & 0xFF0FFF0Fu) | 0x00400040u,
+                                    (__byte_perm(nh, kMagicHi, 0x4140) & 0xFF0FFF0Fu) | 0x00400040u,
+                                    (__byte_perm(nh, kMagicHi, 0x4342) & 0xFF0FFF0Fu) | 0x00400040u};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int k = 8 * c + 2 * q;
-            const uint64_t peer = fma_x2(f32x2(__uint_as_float(__byte_perm(w[q], hb[q], 0x5410)),
-                                               __uint_as_float(__byte_perm(w[q], hb[q], 0x7632))),
-                                         pdec2, pm2);
-            f32x2_split(fma_x2(f32x2(x[k], x[k + 1]), sl22, peer), x[k], x[k + 1]);
+            for (int q = 0; q < 4; ++q) {
+              const int k = 8 * c + 2 * q;
+              const uint64_t peer = fma_x2(f32x2(__uint_as_float(__byte_perm(w[q], hb[q], 0x5410)),
+                                                 __uint_as_float(__byte_perm(w[q], hb[q], 0x7632))),
+                                           pdec2, pm2);
+              f32x2_split(fma_x2(f32x2(x[k], x[k + 1]), sl22, peer), x[k], x[k + 1]);
+            }
+          }
+        } else {
+          const float pdec = pow2i(pe - kXFracBits16), pm = -kMagic16 * pdec;
+          const uint64_t pdec2 = f32x2(pdec, pdec), pm2 = f32x2(pm, pm);
+#pragma unroll
+          for (int c = 0; c < kXLoChunks; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(xbp + c * kXChunk);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int k = 8 * c + 2 * q;
+              const uint64_t peer = fma_x2(f32x2(__uint_as_float(__byte_perm(w[q], kMagicHi16, 0x7610)),
+                                                 __uint_as_float(__byte_perm(w[q], kMagicHi16, 0x7632))),
+                                           pdec2, pm2);
+              f32x2_split(fma_x2(f32x2(x[k], x[k + 1]), sl22, peer), x[k], x[k + 1]);
+            }
           }
         }
         __syncwarp();

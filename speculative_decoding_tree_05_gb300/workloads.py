@@ -410,9 +410,10 @@ def closed_case(kind: str, seed: int = 0xDD7EC000) -> Workload:
     dominant   each query row is 4x one prefix key row (chosen per row): that key's
                score exceeds the others by ~160 nats
     q4, q8     queries scaled by 4 or 8 (partial scores of tens of log2 units)
-    growing    keys drift along one direction that every query shares, so scores
-               grow by ~2 nats per 64 keys (~250 over 8192 keys) and the running max of the online
-               softmax keeps rising across the steps of a key split
+    growing    keys turn towards a direction every query shares, so scores grow by
+               ~2 nats per 64 keys (~250 over 8192 keys) and the running max of the
+               online softmax keeps rising across the steps of a key split; key and
+               value rows stay N(0,1)-sized
     """
     overrides, pattern = CLOSED_CASES[kind]
     kw = dict(max_depth=8, max_branch=0, pool_slots=1 << 16, slots="churn")
@@ -431,14 +432,17 @@ def closed_case(kind: str, seed: int = 0xDD7EC000) -> Workload:
     elif pattern in ("q4", "q8"):
         w.q_bits = pow2_scaled_bits(w.q_bits, 2 if pattern == "q4" else 3)
     elif pattern == "growing":
+        # key j = a_j u + sqrt(1 - a_j^2) g_j with a_j rising from -0.9 to 0.9 (rows stay N(0,1)-sized),
+        # queries = 3.4 u + noise: q.k_j grows linearly with j
         u = rng.standard_normal(D_QK).astype(np.float32)
-        q = bf16_bits_to_f32(w.q_bits) * np.float32(0.25) + u
+        q = bf16_bits_to_f32(w.q_bits) * np.float32(0.25) + np.float32(3.4) * u
         w.q_bits = f32_to_bf16_bits(q.astype(np.float32))
         rows = []
         for b in range(w.batch):
             L = int(w.prefix_len[b])
-            ramp = (np.arange(L, dtype=np.float32) * np.float32(0.00075))[:, None]
-            rows.append(f32_to_bf16_bits(bf16_bits_to_f32(w.kv_prefix_bits[b]) + ramp * u[None, :]))
+            a = np.linspace(-0.9, 0.9, L, dtype=np.float32)[:, None]
+            g = bf16_bits_to_f32(w.kv_prefix_bits[b])
+            rows.append(f32_to_bf16_bits(a * u[None, :] + np.sqrt(np.float32(1) - a * a) * g))
         w.kv_prefix_bits = rows
     w.name = f"closed:{kind}"
     return w
