@@ -8,8 +8,8 @@ header is newer than them.
 build(variant="testhooks") compiles the same sources with test-only hooks into
 lib/libddtree_testhooks.so: short bounded-wait limits, a switch that makes the
 prefix kernel skip the loads of one pipeline step (so a wait runs out and the
-kernel reports DDT_STATUS_TIMEOUT), and a counter of the lazy O rescales.  Only
-tests load it.
+kernel reports DDT_STATUS_TIMEOUT), and counters of the lazy O rescales and of
+the units rerun with 20-bit score exchange.  Only tests load it.
 """
 from __future__ import annotations
 

@@ -209,7 +209,7 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
   float* o_part = reinterpret_cast<float*>(ws + plan.o_off);
 
   if (phases & kPhasePrefix) {
-    if (cudaMemsetAsync(status, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
+    if (cudaMemsetAsync(status, 0, 4 * sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
     if (plan.splits > 0) {
       PrefixParams pp;
 #ifdef DDT_TEST_HOOKS

@@ -41,7 +41,7 @@ struct PrefixParams {
   int32_t block_loads;       // tmap_block and tmap_rope are valid (pool has >= 64 rows)
   float* o_part;             // fp32 [B, max_splits, row_tiles*128, 512]
   float* lse_part;           // fp32 [B, max_splits, row_tiles*128], natural log
-  int32_t* status;           // status word; status[1] counts lazy O rescales in test builds
+  int32_t* status;           // status word; test builds count lazy O rescales in status[1], 20-bit reruns in status[2]
 #ifdef DDT_TEST_HOOKS
   int32_t test_drop_step;    // test builds: producers load nothing for this step of every unit (-1: none)
 #endif

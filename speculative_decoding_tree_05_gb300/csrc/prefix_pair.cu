@@ -28,21 +28,18 @@
 //
 // Partial-score exchange format: per row and 64-key step, block floating point
 // -- one power-of-two exponent e with every |x| < 2^e and 64 mantissas, x being
-// the partial score in log2 units.  Two widths, chosen per warp and step (the
-// receiving warp holds the same 32 rows, so it branches uniformly too):
-//   16-bit  round(x * 2^(14-e)) + 2^15, error <= 2^(e-15), used while every
-//           row of the warp has e <= 4 (error <= 2^-11 log2 units = 3.4e-4 nats;
-//           N(0,1) data at sm_scale 1/sqrt(192) stays there);
-//   20-bit  round(x * 2^(18-e)) + 2^19, error <= 2^(e-19): under 7e-4 nats for
-//           partial scores below 2^9 log2 units (355 nats).  A mantissa travels
-//           as its low 16 bits plus a 4-bit nibble.
-// Either way the log-sum-exp stays within 1e-3 of the exact one even for a
-// dominant key (a 16-bit mantissa alone exceeds 1e-3 nats once partial scores
-// reach 32 log2 units).  The buffer always carries 10 chunks per row (the two
-// nibble chunks are filler in 16-bit mode), so the byte count each receive
-// expects is fixed; the exponent word carries the width (bit 16).  That is at
-// most 2.5 bytes per score instead of fp32's 4: the exchange is bound by DSMEM
-// bandwidth and the shared memory is full.
+// the partial score in log2 units.  Every unit first runs with 16-bit mantissas
+// round(x * 2^(14-e)) + 2^15 (2 bytes per score, the DSMEM budget the step
+// period affords): error <= 2^(e-15), i.e. <= 2^-11 log2 units (3.4e-4 nats)
+// while e <= 4, which N(0,1) data at sm_scale 1/sqrt(192) never leaves.  If
+// any row of either CTA had e > 4 in any step, the pair computes the unit again
+// with 20-bit mantissas round(x * 2^(18-e)) + 2^19 (the low 16 bits plus a
+// packed 4-bit nibble, 2.5 bytes per score): error <= 2^(e-19), under 7e-4 nats
+// for partial scores below 2^9 log2 units (355 nats).  So the log-sum-exp stays
+// within 1e-3 of the exact one even for a dominant key (16-bit mantissas alone
+// exceed 1e-3 nats once partial scores reach 32 log2 units).  The two widths
+// are separate instantiations of the unit: the normal pass carries no code of
+// the wide one, which would cost its issue-bound softmax about a tenth.
 // Rounding to an integer and packing use the float adder: x * 2^(k-e) + M with
 // M = 1.5 * 2^23 + 2^(k+1) is an integer-valued float whose low k+2 bits are
 // the biased mantissa and whose high bits are fixed, so no int/float conversion
@@ -113,6 +110,7 @@ constexpr int kXSets = 2;                                // exchange barrier pai
 constexpr int kXChunk = kTileRows * 16;                  // one 16-byte chunk of every row of the tile
 constexpr int kXLoChunks = kNk * 2 / 16;                 // 8: low 16 bits of the 64 mantissas
 constexpr int kXNibChunks = kNk / 2 / 16;                // 2: their top 4 bits, two per byte
+constexpr int kXLoBytes = kXLoChunks * kXChunk;         // 16384: 16-bit mantissas of one step
 constexpr int kXBytes = (kXLoChunks + kXNibChunks) * kXChunk;  // 20480: 20-bit mantissas of one step
 constexpr int kEBytes = kTileRows * 4;                   // 512: one exponent per row
 constexpr int kQRopeBytes = kTileRows * 64;              // 8192: Q_r rope dims, 64-byte swizzle
@@ -140,8 +138,7 @@ constexpr uint32_t kMagicHi = 0x4B4B4B4Bu;               // top byte of every en
 constexpr int kXFracBits16 = 14;                         // 16-bit mantissa = round(x * 2^(14-e)) + 2^15
 constexpr float kMagic16 = 12615680.0f;                  // 1.5 * 2^23 + 2^15
 constexpr uint32_t kMagicHi16 = 0x4B400000u;             // top half of every 16-bit-encoded float
-constexpr int kX16MaxExp = 4;                            // 16-bit mantissas while every e of the warp is <= 4
-constexpr uint32_t kXWide = 1u << 16;                    // exponent word flag: 20-bit mantissas
+constexpr int kX16MaxExp = 4;                            // 16-bit mantissas suffice while every e is <= 4
 constexpr int kSoftmaxBarrier = 1;                       // named barrier of the 256 softmax threads
 static_assert(kNk == 64, "the step layout assumes 64 keys");
 
@@ -160,6 +157,8 @@ struct Shared {
   volatile int pv_next;       // the step whose P.V is issued next (P.V goes in step order)
   uint32_t tmem_base;
   int abort;
+  int need_wide;              // 16-bit pass: a partial of this CTA needed more than 16-bit mantissas
+  int peer_need_wide;         // the peer CTA's flag word (stored remotely at the end of the 16-bit pass)
 };
 
 // Power-of-two exponent e with |x| < 2^e for every |x| <= amax (amax finite, >= 0).
@@ -170,40 +169,17 @@ __device__ __forceinline__ int block_exponent(float amax) {
 }
 __device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(127 + k) << 23); }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_pair_kernel(const __grid_constant__ PrefixParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared sh;
+// One unit = one CTA pair on one (request, 128-row tile, key split).  kWide
+// selects the exchange width: false = 16-bit mantissas (the normal pass; it
+// returns whether the pair saw a partial needing more), true = 20-bit (a rerun
+// of the same unit, separately compiled so that the normal pass carries none
+// of its code).
+template <bool kWide>
+__device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint8_t* smem_raw, int row_tile,
+                                         int split, int b, int kbegin, int kend, int rows_b) {
   volatile int* abort = &sh.abort;
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
-  // the merge kernel may be scheduled once every CTA of this grid has started:
-  // it then occupies only SMs freed by finished CTAs and waits for this grid
-  // to complete before it reads the partials
-  grid_dep_launch();
-  // x: the pair of a 128-row tile, y: the key split.  CTAs are dispatched in
-  // x-fastest order, so the pairs of one wave share one or two key ranges:
-  // their rows stay in L2 instead of every wave re-reading the whole prefix
-  // from HBM.
-  const int row_tile = blockIdx.x >> 1;
-  const int split = blockIdx.y;
-  const int b = blockIdx.z;
-
-  int L = __ldg(p.prefix_len + b);
-  if (L < 0 || L > p.max_prefix_len) {
-    if (tid == 0 && rank == 0 && split == 0 && row_tile == 0) atomicOr(p.status, kStatusBadPrefix);
-    L = L < 0 ? 0 : p.max_prefix_len;
-  }
-  const int kbegin = split * p.chunk;
-  if (kbegin >= L) return;  // both CTAs of the pair leave together
-  // ragged trees: only the rows of the request's first tree_len[b] nodes are computed
-  int rows_b = p.rows;
-  if (p.tree_len != nullptr) {
-    const int tl = __ldg(p.tree_len + b);
-    rows_b = (tl < 0 ? 0 : (tl > p.nodes ? p.nodes : tl)) * p.heads;  // out-of-range values: the merge reports them
-  }
-  if (row_tile * kTileRows >= rows_b) return;  // a tile of inactive rows: both CTAs leave together
-  const int kend = min(L, kbegin + p.chunk);
   const int ntiles = (kend - kbegin + kNk - 1) / kNk;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -230,11 +206,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     mbar_init(&sh.mma_drain, 3);  // one commit from each MMA-issuing thread
     sh.pv_next = 0;
     sh.abort = 0;
+    sh.need_wide = 0;
+    sh.peer_need_wide = 0;
     fence_mbar_init();
-  }
-  if (warp == 0) {
-    tmem_alloc(&sh.tmem_base, kTmemCols);
-    tmem_relinquish();
   }
   // Global reads that need no set-up are issued before the CTA's barrier, so
   // their latency overlaps it: the producers' slot indices of the first steps
@@ -460,6 +434,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       xbar_remote[i] = mapa_shared(smem_u32(&sh.x_full[i]), peer);
       xfree_remote[i] = mapa_shared(smem_u32(&sh.x_free[i]), peer);
     }
+    bool need_wide = false;  // 16-bit pass: a row's partial of some step had e > kX16MaxExp
     const bool lead = (warp & 3) == 0 && lane == 0;    // row 0 of this set; issues the set's P.V
     const uint64_t d_v = smem_desc(stage0, kLatBlock, 1024, kSwizzle128B);  // V of P.V: MN-major
     float m_used = -CUDART_INF_F;                      // running max after the last step seen
@@ -480,7 +455,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
         sl0 = fetch_slot(j + 2, 0);
         sl1 = fetch_slot(j + 2, 1);
       }
-      if (lead) mbar_arrive_expect_tx(&sh.x_full[xb_i], kXBytes + kEBytes);
+      if (lead) mbar_arrive_expect_tx(&sh.x_full[xb_i], (kWide ? kXBytes : kXLoBytes) + kEBytes);
       if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.s_full[sb], (j / 2) & 1, abort))) { ok = false; break; }
       tc_fence_after();
       float x[64];
@@ -495,9 +470,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
       const float sl2 = p.scale_log2;
       const int e = block_exponent(amax * sl2);
-      const bool wide = __any_sync(0xffffffffu, e > kX16MaxExp);
-      const float enc = sl2 * pow2i((wide ? kXFracBits : kXFracBits16) - e);
-      const float magic = wide ? kMagic : kMagic16;
+      if (!kWide) need_wide |= e > kX16MaxExp;
+      const float enc = sl2 * pow2i((kWide ? kXFracBits : kXFracBits16) - e);
+      const float magic = kWide ? kMagic : kMagic16;
       const uint64_t enc2 = f32x2(enc, enc), magic2 = f32x2(magic, magic);
       // the peer must have read step j-1 (the other set's) out of the buffer before it is overwritten
       if (j >= 1 && !__all_sync(0xffffffffu,
@@ -507,10 +482,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       }
       {
         // chunk-major buffer [10 chunks][128 rows][16 B]: a warp's store of one chunk is 512 contiguous
-        // bytes.  Chunk c < 8 holds the low 16 bits of mantissas 8c..8c+7; in 20-bit mode chunk 8 + c/4,
-        // word c%4, holds their top nibbles (byte i: mantissa 8c+i in the low nibble, 8c+i+4 in the high).
+        // bytes.  Chunk c < 8 holds the low 16 bits of mantissas 8c..8c+7; for 20-bit mantissas chunk
+        // 8 + c/4, word c%4, holds their top nibbles (byte i: mantissa 8c+i in the low nibble, 8c+i+4
+        // in the high one).
         const uint32_t xr = x_remote + r * 16, br = xbar_remote[xb_i];
-        uint32_t nib[4] = {0u, 0u, 0u, 0u};
+        uint32_t nib[4];
 #pragma unroll
         for (int c = 0; c < kXLoChunks; ++c) {
           uint32_t tb[8], w[4];
@@ -524,16 +500,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
             w[q] = __byte_perm(tb[2 * q], tb[2 * q + 1], 0x5410);
           }
           st_async_v4(xr + c * kXChunk, make_uint4(w[0], w[1], w[2], w[3]), br);
-          if (wide) {
+          if (kWide) {
             // bits 16..19 sit in byte 2 of each encoded float (as 0x40 | nibble)
             const uint32_t lo4 = __byte_perm(__byte_perm(tb[0], tb[1], 0x0062), __byte_perm(tb[2], tb[3], 0x6200), 0x7610);
             const uint32_t hi4 = __byte_perm(__byte_perm(tb[4], tb[5], 0x0062), __byte_perm(tb[6], tb[7], 0x6200), 0x7610);
             nib[c & 3] = (lo4 & 0x0F0F0F0Fu) | ((hi4 << 4) & 0xF0F0F0F0u);
+            if ((c & 3) == 3)
+              st_async_v4(xr + (kXLoChunks + (c >> 2)) * kXChunk, make_uint4(nib[0], nib[1], nib[2], nib[3]), br);
           }
-          if ((c & 3) == 3)
-            st_async_v4(xr + (kXLoChunks + (c >> 2)) * kXChunk, make_uint4(nib[0], nib[1], nib[2], nib[3]), br);
         }
-        st_async_b32(e_remote + r * 4, (static_cast<uint32_t>(e) & 0xFFFFu) | (wide ? kXWide : 0u), br);
+        st_async_b32(e_remote + r * 4, static_cast<uint32_t>(e), br);
       }
       // key mask of this step (past the split end or a slot outside the pool)
       const uint32_t masked0 = __ballot_sync(
@@ -548,48 +524,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       float mx = -CUDART_INF_F;
       {
         const uint8_t* xbp = smem + kOffX + r * 16;
-        const uint32_t ew = *reinterpret_cast<const uint32_t*>(smem + kOffE + r * 4);
-        const int pe = static_cast<int16_t>(ew & 0xFFFFu);
-        const uint64_t sl22 = f32x2(sl2, sl2);
-        if (ew & kXWide) {
-          const float pdec = pow2i(pe - kXFracBits), pm = -kMagic * pdec;
-          const uint64_t pdec2 = f32x2(pdec, pdec), pm2 = f32x2(pm, pm);
-          uint4 nv = *reinterpret_cast<const uint4*>(xbp + kXLoChunks * kXChunk);
+        const int pe = *reinterpret_cast<const int*>(smem + kOffE + r * 4);
+        // the low 16 bits, as (lo - bias) * 2^(e-f): f = 14, bias 2^15 (16-bit) or f = 18, bias 2^19 (20-bit)
+        const float pdec = pow2i(pe - (kWide ? kXFracBits : kXFracBits16)), pm = -(kWide ? kMagic : kMagic16) * pdec;
+        const uint64_t pdec2 = f32x2(pdec, pdec), pm2 = f32x2(pm, pm), sl22 = f32x2(sl2, sl2);
 #pragma unroll
-          for (int c = 0; c < kXLoChunks; ++c) {
-            if (c == 4) nv = *reinterpret_cast<const uint4*>(xbp + (kXLoChunks + 1) * kXChunk);
-            const uint4 v = *reinterpret_cast<const uint4*>(xbp + c * kXChunk);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            const uint32_t nb = (c & 3) == 0 ? nv.x : (c & 3) == 1 ? nv.y : (c & 3) == 2 ? nv.z : nv.w;
-            const uint32_t nh = nb >> 4;
-            // byte 2 and 3 of each float: 0x40 | nibble, 0x4B (two mantissas per word)
-            const uint32_t hb[4] = {(__byte_perm(nb, kMagicHi, 0x4140) & 0xFF0FFF0Fu) | 0x00400040u,
-                                    (__byte_perm(nb, kMagicHi, 0x4342) & 0xFF0FFF0Fu) | 0x00400040u,
-                                    (__byte_perm(nh, kMagicHi, 0x4140) & 0xFF0FFF0Fu) | 0x00400040u,
-                                    (__byte_perm(nh, kMagicHi, 0x4342) & 0xFF0FFF0Fu) | 0x00400040u};
+        for (int c = 0; c < kXLoChunks; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xbp + c * kXChunk);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int k = 8 * c + 2 * q;
-              const uint64_t peer = fma_x2(f32x2(__uint_as_float(__byte_perm(w[q], hb[q], 0x5410)),
-                                                 __uint_as_float(__byte_perm(w[q], hb[q], 0x7632))),
-                                           pdec2, pm2);
-              f32x2_split(fma_x2(f32x2(x[k], x[k + 1]), sl22, peer), x[k], x[k + 1]);
-            }
+          for (int q = 0; q < 4; ++q) {
+            const int k = 8 * c + 2 * q;
+            const uint64_t peer = fma_x2(f32x2(__uint_as_float(__byte_perm(w[q], kMagicHi16, 0x7610)),
+                                               __uint_as_float(__byte_perm(w[q], kMagicHi16, 0x7632))),
+                                         pdec2, pm2);
+            f32x2_split(fma_x2(f32x2(x[k], x[k + 1]), sl22, peer), x[k], x[k + 1]);
           }
-        } else {
-          const float pdec = pow2i(pe - kXFracBits16), pm = -kMagic16 * pdec;
-          const uint64_t pdec2 = f32x2(pdec, pdec), pm2 = f32x2(pm, pm);
+        }
+        if (kWide) {
+          // 20-bit mantissas: add nibble * 2^16 * 2^(e-18)
+          const float cs = pow2i(pe - 2), cb = -12582912.0f * cs;  // nibble n as float bits 0x4B4000nn = 1.5 * 2^23 + n
+          const uint64_t cs2 = f32x2(cs, cs), cb2 = f32x2(cb, cb);
 #pragma unroll
-          for (int c = 0; c < kXLoChunks; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(xbp + c * kXChunk);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          for (int h = 0; h < 2; ++h) {
+            const uint4 nv = *reinterpret_cast<const uint4*>(xbp + (kXLoChunks + h) * kXChunk);
+            const uint32_t nw[4] = {nv.x, nv.y, nv.z, nv.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int k = 8 * c + 2 * q;
-              const uint64_t peer = fma_x2(f32x2(__uint_as_float(__byte_perm(w[q], kMagicHi16, 0x7610)),
-                                                 __uint_as_float(__byte_perm(w[q], kMagicHi16, 0x7632))),
-                                           pdec2, pm2);
-              f32x2_split(fma_x2(f32x2(x[k], x[k + 1]), sl22, peer), x[k], x[k + 1]);
+            for (int cc = 0; cc < 4; ++cc) {
+              const int c = 4 * h + cc;
+              const uint32_t lo = nw[cc] & 0x0F0F0F0Fu, hi = (nw[cc] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+              for (int i = 0; i < 4; i += 2) {
+                // mantissas 8c+i, 8c+i+1 (low nibbles) and 8c+i+4, 8c+i+5 (high nibbles)
+                const uint64_t nl = f32x2(__uint_as_float(__byte_perm(lo, 0x4B400000u, 0x7640 + i)),
+                                          __uint_as_float(__byte_perm(lo, 0x4B400000u, 0x7641 + i)));
+                const uint64_t nh = f32x2(__uint_as_float(__byte_perm(hi, 0x4B400000u, 0x7640 + i)),
+                                          __uint_as_float(__byte_perm(hi, 0x4B400000u, 0x7641 + i)));
+                const int k = 8 * c + i;
+                f32x2_split(add_x2(f32x2(x[k], x[k + 1]), fma_x2(nl, cs2, cb2)), x[k], x[k + 1]);
+                f32x2_split(add_x2(f32x2(x[k + 4], x[k + 5]), fma_x2(nh, cs2, cb2)), x[k + 4], x[k + 5]);
+              }
             }
           }
         }
@@ -697,6 +671,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
       }
     }
 
+    if (!kWide && __any_sync(0xffffffffu, need_wide) && lane == 0) sh.need_wide = 1;
     // epilogue: combine both sets' row sums, wait for the last P.V, then
     // o = O / l (set s writes O columns [128 s, 128 s + 128)) and lse.
     // The row state shares the exchange buffer: write it only once both sets
@@ -760,10 +735,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     // wait for them (bounded) before the shared memory is released
     for (int t = max(0, issued - kStages); t < issued; ++t) mbar_wait(&sh.k_full[t % kStages], (t / kStages) & 1);
   }
-  cluster_sync();  // no CTA leaves while its peer may still write into its shared memory
+  // The pair's 16-bit pass decides together whether to rerun with 20-bit
+  // mantissas: each CTA sends the peer its flag word (bit 0: a partial needed
+  // more than 16 bits, bit 1: this CTA gave up on a wait), and the unit is
+  // rerun only if some partial needed it and neither CTA aborted (copies of an
+  // aborted pass may still be landing, so its barriers are not set up again).
+  if (!kWide && tid == 0)
+    st_shared_cluster_b32(mapa_shared(smem_u32(&sh.peer_need_wide), rank ^ 1u), sh.need_wide | (*abort ? 2 : 0));
+  cluster_sync();  // no CTA leaves (or starts another pass) while its peer may still write into its shared memory
+  if (kWide) return false;
+  const int flags = sh.need_wide | (*abort ? 2 : 0) | sh.peer_need_wide;
+  __syncthreads();  // every thread has read the flags before a second pass resets them
+  return flags == 1;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_pair_kernel(const __grid_constant__ PrefixParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Shared sh;
+  const int tid = threadIdx.x;
+  const uint32_t rank = cluster_ctarank();
+  // the merge kernel may be scheduled once every CTA of this grid has started:
+  // it then occupies only SMs freed by finished CTAs and waits for this grid
+  // to complete before it reads the partials
+  grid_dep_launch();
+  // x: the pair of a 128-row tile, y: the key split.  CTAs are dispatched in
+  // x-fastest order, so the pairs of one wave share one or two key ranges:
+  // their rows stay in L2 instead of every wave re-reading the whole prefix
+  // from HBM.
+  const int row_tile = blockIdx.x >> 1;
+  const int split = blockIdx.y;
+  const int b = blockIdx.z;
+
+  int L = __ldg(p.prefix_len + b);
+  if (L < 0 || L > p.max_prefix_len) {
+    if (tid == 0 && rank == 0 && split == 0 && row_tile == 0) atomicOr(p.status, kStatusBadPrefix);
+    L = L < 0 ? 0 : p.max_prefix_len;
+  }
+  const int kbegin = split * p.chunk;
+  if (kbegin >= L) return;  // both CTAs of the pair leave together
+  // ragged trees: only the rows of the request's first tree_len[b] nodes are computed
+  int rows_b = p.rows;
+  if (p.tree_len != nullptr) {
+    const int tl = __ldg(p.tree_len + b);
+    rows_b = (tl < 0 ? 0 : (tl > p.nodes ? p.nodes : tl)) * p.heads;  // out-of-range values: the merge reports them
+  }
+  if (row_tile * kTileRows >= rows_b) return;  // a tile of inactive rows: both CTAs leave together
+  const int kend = min(L, kbegin + p.chunk);
+  // 16-bit exchange first; the rare unit whose partial scores are too large for
+  // it (both CTAs get the same answer) is computed again with 20-bit mantissas
+  // and its partial result overwritten
+  // TMEM is allocated once for both passes (after relinquishing the allocation
+  // permit a CTA may not allocate again); each pass's MMAs have drained before
+  // it returns.
+  const int warp = tid >> 5;
+  if (warp == 0) {
+    tmem_alloc(&sh.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (run_unit<false>(p, sh, smem_raw, row_tile, split, b, kbegin, kend, rows_b)) {
+#ifdef DDT_TEST_HOOKS
+    if (tid == 0 && rank == 0) atomicAdd(p.status + 2, 1);  // test builds count the 20-bit reruns
+#endif
+    run_unit<true>(p, sh, smem_raw, row_tile, split, b, kbegin, kend, rows_b);
+  }
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(sh.tmem_base, kTmemCols);
   }
 }
 

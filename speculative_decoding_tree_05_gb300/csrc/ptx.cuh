@@ -143,6 +143,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint4 v, uint3
                : "memory");
 }
 
+// Plain 4-byte store into a peer CTA's shared memory (visible to the peer after
+// a cluster barrier).
+__device__ __forceinline__ void st_shared_cluster_b32(uint32_t remote_addr, int v) {
+  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(remote_addr), "r"(v) : "memory");
+}
+
 // 4-byte variant of st_async_v4.
 __device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr), "r"(v),

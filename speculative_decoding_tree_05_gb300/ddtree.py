@@ -70,9 +70,10 @@ def load(path: str):
                                                     ctypes.POINTER(Dims), vp]
     L.ddtree_kv_compact.restype = ctypes.c_int
     L.ddtree_kv_compact.argtypes = [vp, vp, i32p, i32p, vp, i32p, ctypes.POINTER(Dims), vp, vp]
-    L.ddtree_kv_compact_check.restype = ctypes.c_int
-    L.ddtree_kv_compact_check.argtypes = [vp, vp, vp, vp, ctypes.POINTER(Dims), ctypes.c_int32,
-                                          ctypes.POINTER(ctypes.c_int64)]
+    if hasattr(L, "ddtree_kv_compact_check"):   # absent from builds that predate the validator
+        L.ddtree_kv_compact_check.restype = ctypes.c_int
+        L.ddtree_kv_compact_check.argtypes = [vp, vp, vp, vp, ctypes.POINTER(Dims), ctypes.c_int32,
+                                              ctypes.POINTER(ctypes.c_int64)]
     L.ddtree_read_device_status.restype = ctypes.c_int
     L.ddtree_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
     L.ddtree_status_string.restype = ctypes.c_char_p

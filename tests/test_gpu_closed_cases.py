@@ -14,8 +14,10 @@ fp64 oracle (whose own pins cover the same closed forms on the CPU):
   growing_scores  scores rise by ~2 nats per 64-key step, so the running max keeps
                   growing inside a key split and the lazy O rescale runs repeatedly
 A test build of the library (short wait limits, test hooks) checks that the lazy
-rescale really runs on the growing case, and that a bounded wait which runs out
-reports DDT_STATUS_TIMEOUT and leaves the context usable.
+rescale really runs on the growing case, that units whose partial scores
+outgrow 16-bit exchange mantissas are rerun with 20-bit ones (and N(0,1) data
+never is), and that a bounded wait which runs out reports DDT_STATUS_TIMEOUT
+and leaves the context usable.
 """
 import numpy as np
 import pytest
@@ -69,6 +71,25 @@ def test_lazy_rescale_runs_and_matches(testhooks):
     # the product build gives the same bits (the counter is the only difference)
     out2, lse2, st2, _, _ = run_gpu(w)
     assert st2 == 0 and torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def _reruns(v):
+    return int(v.workspace[8:12].view(torch.int32).item())
+
+
+@pytest.mark.parametrize("kind", ["q_x4", "q_x8", "dominant_key", "growing_scores"])
+def test_large_scores_rerun_with_wide_exchange(testhooks, kind):
+    w = wl.closed_case(kind)
+    out, lse, st, _, v = run_gpu(w, library=testhooks)
+    assert st == 0 and _reruns(v) > 0
+    ref_o, ref_l, _ = oracle.verify_workload(w)
+    compare(out, lse, ref_o, ref_l)
+
+
+def test_unit_scale_scores_never_rerun(testhooks):
+    w = wl.make_workload("c2")
+    _, _, st, _, v = run_gpu(w, library=testhooks)
+    assert st == 0 and _reruns(v) == 0
 
 
 def test_timeout_is_reported_and_the_next_call_is_correct(testhooks):
