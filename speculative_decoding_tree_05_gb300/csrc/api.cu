@@ -2,6 +2,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <mutex>
 #include <utility>
@@ -46,7 +47,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Plan {
   int rows = 0, row_tiles = 0, chunk = kKeysPerTile, splits = 0;
-  size_t lse_off = 0, o_off = 0, bytes = 0;
+  size_t cnt_off = 0, cnt_bytes = 0, lse_off = 0, o_off = 0, bytes = 0;
 };
 
 int check_dims(const ddt_dims* d) {
@@ -104,7 +105,10 @@ int make_plan(const ddt_dims* d, int sm_count, Plan* plan) {
     p.splits = static_cast<int>((L + chunk - 1) / chunk);
   }
   const size_t part_rows = size_t(d->batch) * p.splits * p.row_tiles * kTileRows;
-  p.lse_off = kStatusBytes;
+  // [status words | split arrivals per (request, row tile) | lse partials | o partials]
+  p.cnt_off = kStatusBytes;
+  p.cnt_bytes = size_t(d->batch) * p.row_tiles * sizeof(int32_t);
+  p.lse_off = align_up(p.cnt_off + p.cnt_bytes, 256);
   p.o_off = align_up(p.lse_off + part_rows * sizeof(float), 256);
   p.bytes = p.o_off + part_rows * kDv * sizeof(float);
   *plan = p;
@@ -179,7 +183,7 @@ extern "C" size_t ddtree_verify_workspace_bytes(const ddt_dims* dims) {
 namespace ddt {
 namespace {
 
-enum Phase : int { kPhasePrefix = 1, kPhaseMerge = 2 };
+enum Phase : int { kPhasePrefix = 1, kPhaseMerge = 2, kPhaseFused = 4 };
 
 int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t* slot_idx,
                   const int32_t* prefix_len, const int32_t* tree_parent, const int32_t* tree_slot_idx,
@@ -208,9 +212,11 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
   float* lse_part = reinterpret_cast<float*>(ws + plan.lse_off);
   float* o_part = reinterpret_cast<float*>(ws + plan.o_off);
 
-  if (phases & kPhasePrefix) {
-    if (cudaMemsetAsync(status, 0, 4 * sizeof(int32_t), s) != cudaSuccess) return DDT_ERR_LAUNCH;
-    if (plan.splits > 0) {
+  if (phases & (kPhasePrefix | kPhaseFused)) {
+    // the status words and (fused) the split arrival counters start at zero
+    const size_t clear = (phases & kPhaseFused) ? plan.cnt_off + plan.cnt_bytes : 4 * sizeof(int32_t);
+    if (cudaMemsetAsync(status, 0, clear, s) != cudaSuccess) return DDT_ERR_LAUNCH;
+    if (plan.splits > 0 || (phases & kPhaseFused)) {
       PrefixParams pp;
 #ifdef DDT_TEST_HOOKS
       pp.test_drop_step = g_test_drop_step;
@@ -239,6 +245,24 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
       pp.o_part = o_part;
       pp.lse_part = lse_part;
       pp.status = status;
+      if (phases & kPhaseFused) {
+        FusedParams fp;
+        fp.pre = pp;
+        fp.tree_parent = tree_parent;
+        fp.tree_slot_idx = tree_slot_idx;
+        fp.out = out;
+        fp.lse = lse;
+        fp.arrivals = reinterpret_cast<int32_t*>(ws + plan.cnt_off);
+        fp.splits = plan.splits > 0 ? plan.splits : 1;  // an empty prefix still has a (tail-only) unit per tile
+        const int64_t units = int64_t(dims->batch) * fp.splits * plan.row_tiles;
+        if (units > INT32_MAX) return DDT_ERR_DIMS;
+        fp.units = static_cast<int32_t>(units);
+        int pairs = fused_max_pairs();
+        if (pairs <= 0) pairs = dev.sm_count >= 2 ? dev.sm_count / 2 : 1;
+        if (pairs > fp.units) pairs = fp.units;
+        if (launch_fused(fp, pairs, s) != cudaSuccess) return DDT_ERR_LAUNCH;
+        return DDT_OK;
+      }
       if (launch_prefix(pp, dims->batch, plan.splits, s) != cudaSuccess) return DDT_ERR_LAUNCH;
     }
   }
@@ -280,17 +304,15 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
   q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, nullptr, sm_scale, out, lse, dims, workspace, \
       workspace_bytes, stream
 
-extern "C" int ddtree_verify_attn(DDT_VERIFY_ARGS) {
-  return verify_phases(kPhasePrefix | kPhaseMerge, DDT_VERIFY_PASS);
-}
+extern "C" int ddtree_verify_attn(DDT_VERIFY_ARGS) { return verify_phases(kPhaseFused, DDT_VERIFY_PASS); }
 extern "C" int ddtree_verify_attn_ragged(const void* q, const void* kv_pool, const int32_t* slot_idx,
                                          const int32_t* prefix_len, const int32_t* tree_parent,
                                          const int32_t* tree_slot_idx, const int32_t* tree_len, float sm_scale,
                                          float* out, float* lse, const ddt_dims* dims, void* workspace,
                                          size_t workspace_bytes, ddt_stream_t stream) {
   if (!tree_len && dims && dims->batch > 0) return DDT_ERR_NULL;
-  return verify_phases(kPhasePrefix | kPhaseMerge, q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx,
-                       tree_len, sm_scale, out, lse, dims, workspace, workspace_bytes, stream);
+  return verify_phases(kPhaseFused, q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, tree_len, sm_scale,
+                       out, lse, dims, workspace, workspace_bytes, stream);
 }
 extern "C" int ddtree_verify_prefix_phase(DDT_VERIFY_ARGS) { return verify_phases(kPhasePrefix, DDT_VERIFY_PASS); }
 extern "C" int ddtree_verify_merge_phase(DDT_VERIFY_ARGS) { return verify_phases(kPhaseMerge, DDT_VERIFY_PASS); }

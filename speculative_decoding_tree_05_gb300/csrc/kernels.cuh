@@ -71,6 +71,20 @@ struct TailParams {
   int32_t* status;
 };
 
+// Fused verify: one persistent launch of CTA pairs that loop over the units
+// (request, key split, 128-row tile) of the prefix pass; the pair completing the
+// last split of a (request, row tile) merges that tile (tree tail + log-sum-exp).
+struct FusedParams {
+  PrefixParams pre;             // the prefix pass of every unit (o_part, lse_part, status inside)
+  const int32_t* tree_parent;   // [B, T]
+  const int32_t* tree_slot_idx; // [B, T]
+  float* out;                   // fp32 [B, T, H, 512]
+  float* lse;                   // fp32 [B, T, H]
+  int32_t* arrivals;            // [B, row_tiles] splits finished per (request, row tile); zero at launch
+  int32_t units;                // B * splits * row_tiles
+  int32_t splits;               // key-split slots per request (>= 1)
+};
+
 struct CompactParams {
   const uint16_t* src;
   uint16_t* dst;
@@ -95,6 +109,9 @@ cudaError_t configure_prefix();
 cudaError_t configure_tail_merge();
 
 cudaError_t launch_prefix(const PrefixParams& p, int batch, int splits, cudaStream_t stream);
+// pairs: CTA pairs of the persistent grid (at most the clusters that fit at once)
+cudaError_t launch_fused(const FusedParams& p, int pairs, cudaStream_t stream);
+int fused_max_pairs();  // co-resident CTA pairs of the fused kernel on the current device (0: unknown)
 cudaError_t launch_tail_merge(const TailParams& p, int batch, cudaStream_t stream);
 cudaError_t launch_kv_compact(const CompactParams& p, int batch, cudaStream_t stream);
 

@@ -92,6 +92,7 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include "kernels.cuh"
+#include "merge_row.cuh"
 #include "ptx.cuh"
 
 namespace ddt {
@@ -157,6 +158,7 @@ struct Shared {
   volatile int pv_next;       // the step whose P.V is issued next (P.V goes in step order)
   uint32_t tmem_base;
   int abort;
+  int last_arrival;           // fused kernel: this pair finished the last split of its (request, row tile)
   int need_wide;              // 16-bit pass: a partial of this CTA needed more than 16-bit mantissas
   int peer_need_wide;         // the peer CTA's flag word (stored remotely at the end of the 16-bit pass)
 };
@@ -169,14 +171,47 @@ __device__ __forceinline__ int block_exponent(float amax) {
 }
 __device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(127 + k) << 23); }
 
-// One unit = one CTA pair on one (request, 128-row tile, key split).  kWide
-// selects the exchange width: false = 16-bit mantissas (the normal pass; it
-// returns whether the pair saw a partial needing more), true = 20-bit (a rerun
-// of the same unit, separately compiled so that the normal pass carries none
-// of its code).
+// Barriers of a CTA, set up once per launch: their phases then run on across
+// the passes and units a CTA computes (step g of the CTA uses stage g % 5, S
+// buffer and softmax set g % 2, ...), so an arrival that lands late -- a
+// tensor-core commit or a remote arrive of the previous pass -- still counts in
+// the phase it belongs to.  The first run_unit's set-up barriers publish them
+// to the peer before any remote access.
+__device__ __forceinline__ void init_barriers(Shared& sh) {
+  for (int i = 0; i < kStages; ++i) {
+    mbar_init(&sh.k_full[i], kProducers + 1);  // every producer thread + one (TMA) arrival
+    mbar_init(&sh.k_empty[i], 1);
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&sh.s_full[i], 1);
+    mbar_init(&sh.s_free[i], 128);
+    mbar_init(&sh.p_ready[i], 128);
+    mbar_init(&sh.m_ready[i], 128);
+  }
+  for (int i = 0; i < kXSets; ++i) {
+    mbar_init(&sh.x_full[i], 1);
+    mbar_init(&sh.x_free[i], 4);  // the 4 warps of the peer's set
+  }
+  mbar_init(&sh.q_ready, 256);
+  mbar_init(&sh.mma_drain, 3);  // one commit from each MMA-issuing thread, per pass
+  sh.pv_next = 0;
+  sh.abort = 0;
+  fence_mbar_init();
+}
+
+constexpr int kUnitWide = 1;     // run_unit result: a partial of the 16-bit pass needed wider mantissas
+constexpr int kUnitAborted = 2;  // run_unit result: a CTA of the pair gave up on a wait
+
+// One pass over one unit = one CTA pair on one (request, 128-row tile, key
+// split), as the CTA's steps G .. G + ntiles - 1 and its pass number `pass`.
+// kWide selects the exchange width: false = 16-bit mantissas (the normal pass),
+// true = 20-bit (a rerun of the same unit, separately compiled so that the
+// normal pass carries none of its code).  Returns the pair's kUnit* flags (the
+// same in both CTAs): after kUnitAborted the CTA's barriers are in an unknown
+// state and it must not run another pass.
 template <bool kWide>
-__device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint8_t* smem_raw, int row_tile,
-                                         int split, int b, int kbegin, int kend, int rows_b) {
+__device__ __forceinline__ int run_unit(const PrefixParams& p, Shared& sh, uint8_t* smem_raw, int row_tile,
+                                        int split, int b, int kbegin, int kend, int rows_b, int G, int pass) {
   volatile int* abort = &sh.abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
@@ -188,27 +223,8 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
   const uint32_t qrope_s = smem_u32(qrope);
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sh.k_full[i], kProducers + 1);  // every producer thread + one (TMA) arrival
-      mbar_init(&sh.k_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sh.s_full[i], 1);
-      mbar_init(&sh.s_free[i], 128);
-      mbar_init(&sh.p_ready[i], 128);
-      mbar_init(&sh.m_ready[i], 128);
-    }
-    for (int i = 0; i < kXSets; ++i) {
-      mbar_init(&sh.x_full[i], 1);
-      mbar_init(&sh.x_free[i], 4);  // the 4 warps of the peer's set
-    }
-    mbar_init(&sh.q_ready, 256);
-    mbar_init(&sh.mma_drain, 3);  // one commit from each MMA-issuing thread
-    sh.pv_next = 0;
-    sh.abort = 0;
     sh.need_wide = 0;
     sh.peer_need_wide = 0;
-    fence_mbar_init();
   }
   // Global reads that need no set-up are issued before the CTA's barrier, so
   // their latency overlaps it: the producers' slot indices of the first steps
@@ -233,7 +249,7 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
 #pragma unroll
   for (int c = 0; c < 4; ++c) qv[16 + c] = q_valid && warp < 8 ? __ldg(qsrc + 64 + 4 * rank + c) : make_uint4(0, 0, 0, 0);
   tc_fence_before();
-  __syncthreads();  // this CTA's barriers initialised and its TMEM allocated
+  __syncthreads();  // this CTA's barriers initialised (first pass), its TMEM allocated and the last pass done
   // The peer addresses this CTA's barriers only after its own cluster_wait,
   // which follows this arrive: threads that touch the peer wait before their
   // first remote access, the others before the final cluster barrier.
@@ -241,7 +257,7 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
   bool ok = true;
-  int issued = 0;  // producers: steps this warp has issued loads for
+  int issued = G;  // producers: the CTA step after the last one this warp has issued loads for
 
   if (warp == 0) {
     // ------------------------------------------------------------------ S issuer
@@ -250,7 +266,7 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
     // a P.V group: this thread issues only S, sleeping on the barrier it needs;
     // each softmax set issues the P.V of its own steps.
     if (lane == 0) {
-      if (!mbar_wait_abortable(&sh.q_ready, 0, abort)) ok = false;
+      if (!mbar_wait_abortable(&sh.q_ready, pass & 1, abort, false, __LINE__)) ok = false;
       fence_proxy_async_smem();  // Q rope dims were stored to shared memory by the softmax threads
       tc_fence_after();
       // operand descriptors of stage 0, built once; a stage or k-step is an offset
@@ -258,10 +274,10 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
       const uint64_t d_rope = smem_desc(stage0 + 4 * kLatBlock, 16, 512, kSwizzle64B);
       const uint64_t d_qrope = smem_desc(qrope_s, 16, 512, kSwizzle64B);
       const uint64_t d_qlat = smem_desc(stage0 + kOffQLat, 16, 1024, kSwizzle128B);
-      for (int ns = 0; ok && ns < ntiles; ++ns) {
+      for (int ns = G; ok && ns < G + ntiles; ++ns) {
         // stage loaded, and S(ns-2) read out of S buffer ns % 2
-        if (!mbar_wait_abortable(&sh.k_full[ns % kStages], (ns / kStages) & 1, abort) ||
-            (ns > 1 && !mbar_wait_abortable(&sh.s_free[ns % 2], ((ns - 2) / 2) & 1, abort))) {
+        if (!mbar_wait_abortable(&sh.k_full[ns % kStages], (ns / kStages) & 1, abort, false, __LINE__) ||
+            (ns > 1 && !mbar_wait_abortable(&sh.s_free[ns % 2], ((ns - 2) / 2) & 1, abort, false, __LINE__))) {
           ok = false;
           break;
         }
@@ -287,7 +303,7 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
       }
       // nothing of this thread's may still be running when TMEM is released (also after a timeout)
       mma_commit(&sh.mma_drain);
-      mbar_wait(&sh.mma_drain, 0);
+      mbar_wait(&sh.mma_drain, pass & 1);
     }
     __syncwarp();
     cluster_wait();
@@ -307,18 +323,19 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
     // slot indices are fetched kSlotLookahead steps ahead: under a gather-heavy
     // load their latency exceeds a step
     for (int j = 0; j < ntiles; ++j) {
+      const int g = G + j;  // the CTA's step
       const int cur0 = pf[0], cur1 = pf[1];
 #pragma unroll
       for (int i = 0; i + 2 < 2 * kSlotLookahead; ++i) pf[i] = pf[i + 2];
       pf[2 * kSlotLookahead - 2] = fetch(j + kSlotLookahead, 0);
       pf[2 * kSlotLookahead - 1] = fetch(j + kSlotLookahead, 1);
-      const int st = j % kStages;
+      const int st = g % kStages;
 #ifdef DDT_TEST_HOOKS
       // test builds: a stage that is never loaded, so the waits for it run out
       if (j == p.test_drop_step) continue;
 #endif
       // warp-uniform wait: the lane shuffles below need every lane
-      const bool waited = j < kStages || mbar_wait_abortable(&sh.k_empty[st], ((j / kStages) - 1) & 1, abort);
+      const bool waited = g < kStages || mbar_wait_abortable(&sh.k_empty[st], ((g / kStages) - 1) & 1, abort, false, __LINE__);
       if (!__all_sync(0xffffffffu, waited)) {
         ok = false;
         break;
@@ -382,7 +399,7 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
         }
       }
       cp_async_arrive_noinc(&sh.k_full[st]);
-      issued = j + 1;
+      issued = g + 1;
     }
     cp_async_wait<0>();
     cluster_wait();
@@ -443,12 +460,15 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
       const int key = kbegin + j * kNk + lane + 32 * e;
       return key < kend ? __ldg(slots + key) : 0;
     };
-    int sl0 = fetch_slot(set, 0), sl1 = fetch_slot(set, 1);
+    // set s takes the CTA steps g with g % 2 == s; j = g - G is the step within the unit
+    const int j0 = (set ^ G) & 1;
+    int sl0 = fetch_slot(j0, 0), sl1 = fetch_slot(j0, 1);
 
-    // Step t uses exchange buffer t % 2 (this set's) in both CTAs.
-    for (int j = set; ok && j < ntiles; j += 2) {
-      const int sb = j % 2;
-      const int xb_i = j % kXSets;                      // this set's exchange barriers
+    // Step g uses exchange barriers g % 2 (this set's) in both CTAs.
+    for (int j = j0; ok && j < ntiles; j += 2) {
+      const int g = G + j;
+      const int sb = g % 2;
+      const int xb_i = g % kXSets;                      // this set's exchange barriers
       const int kbase = kbegin + j * kNk;
       const int cur0 = sl0, cur1 = sl1;
       if (j + 2 < ntiles) {
@@ -456,7 +476,7 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
         sl1 = fetch_slot(j + 2, 1);
       }
       if (lead) mbar_arrive_expect_tx(&sh.x_full[xb_i], (kWide ? kXBytes : kXLoBytes) + kEBytes);
-      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.s_full[sb], (j / 2) & 1, abort))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.s_full[sb], (g / 2) & 1, abort, false, __LINE__))) { ok = false; break; }
       tc_fence_after();
       float x[64];
       tmem_ld32(tmem + lane_off + kColS + sb * kNk, *reinterpret_cast<float(*)[32]>(&x[0]));
@@ -475,8 +495,8 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
       const float magic = kWide ? kMagic : kMagic16;
       const uint64_t enc2 = f32x2(enc, enc), magic2 = f32x2(magic, magic);
       // the peer must have read step j-1 (the other set's) out of the buffer before it is overwritten
-      if (j >= 1 && !__all_sync(0xffffffffu,
-                                mbar_wait_abortable(&sh.x_free[xb_i ^ 1], ((j - 1) / 2) & 1, abort, true))) {
+      if (g >= 1 && !__all_sync(0xffffffffu,
+                                mbar_wait_abortable(&sh.x_free[xb_i ^ 1], ((g - 1) / 2) & 1, abort, true, __LINE__))) {
         ok = false;
         break;
       }
@@ -516,7 +536,7 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
           0xffffffffu, kbase + lane >= kend || cur0 < 0 || static_cast<int64_t>(cur0) >= p.pool_slots);
       const uint32_t masked1 = __ballot_sync(
           0xffffffffu, kbase + lane + 32 >= kend || cur1 < 0 || static_cast<int64_t>(cur1) >= p.pool_slots);
-      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_full[xb_i], (j / kXSets) & 1, abort, true))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.x_full[xb_i], (g / kXSets) & 1, abort, true, __LINE__))) {
         ok = false;
         break;
       }
@@ -579,13 +599,14 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
         for (int k = 0; k < 64; k += 2) mq[(k >> 1) & 3] = fmax3(mq[(k >> 1) & 3], x[k], x[k + 1]);
         mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       }
-      // running max after step j-1 comes from the other set
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.m_ready[(j - 1) % 2], ((j - 1) / 2) & 1, abort))) {
+      // running max after step g-1 comes from the other set (the wait also keeps that set
+      // from overwriting the handoff slot early; a unit's first step starts from -inf)
+      if (g > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait_abortable(&sh.m_ready[(g - 1) % 2], ((g - 1) / 2) & 1, abort, false, __LINE__))) {
           ok = false;
           break;
         }
-        m_used = hand[((j - 1) % 2) * kTileRows + r];
+        if (j > 0) m_used = hand[((g - 1) % 2) * kTileRows + r];
       }
       const float m_prev = m_used;
       if (mx > m_used + kRescaleThreshold) m_used = mx;
@@ -596,9 +617,9 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
 #ifdef DDT_TEST_HOOKS
         if (lane == 0) atomicAdd(p.status + 1, 1);  // test builds count the lazy O rescales
 #endif
-        // O must hold every earlier step: wait for P.V of step j-1 (MMAs complete in order)
+        // O must hold every earlier step: wait for P.V of step g-1 (MMAs complete in order)
         if (!__all_sync(0xffffffffu,
-                        mbar_wait_abortable(&sh.k_empty[(j - 1) % kStages], ((j - 1) / kStages) & 1, abort))) {
+                        mbar_wait_abortable(&sh.k_empty[(g - 1) % kStages], ((g - 1) / kStages) & 1, abort, false, __LINE__))) {
           ok = false;
           break;
         }
@@ -633,10 +654,10 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
       f32x2_split(sq[0], s0, s1);
       f32x2_split(sq[1], s2, s3);
       l += (s0 + s1) + (s2 + s3);
-      // the P buffer was last read by P.V of step j-1
-      if (j >= 1) {
+      // the P buffer was last read by P.V of step g-1
+      if (g >= 1) {
         if (!__all_sync(0xffffffffu,
-                        mbar_wait_abortable(&sh.k_empty[(j - 1) % kStages], ((j - 1) / kStages) & 1, abort))) {
+                        mbar_wait_abortable(&sh.k_empty[(g - 1) % kStages], ((g - 1) / kStages) & 1, abort, false, __LINE__))) {
           ok = false;
           break;
         }
@@ -651,18 +672,25 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
       // k_empty[stage] also tells everyone that P.V(j) is done.
       bool pv_ok = true;
       if (lead) {
-        pv_ok = mbar_wait_abortable(&sh.p_ready[sb], (j / 2) & 1, abort);
-        for (uint32_t spin = 0; pv_ok && sh.pv_next != j; ++spin)
-          if (spin > 4 * DDT_WAIT_LIMIT || ((spin & 255) == 255 && *abort)) pv_ok = false;
+        pv_ok = mbar_wait_abortable(&sh.p_ready[sb], (g / 2) & 1, abort, false, __LINE__);
+        for (uint32_t spin = 0; pv_ok && sh.pv_next != g; ++spin) {
+          if (spin > 4 * DDT_WAIT_LIMIT) {
+#ifdef DDT_TEST_HOOKS
+            atomicCAS(&g_timeout_site, 0u, static_cast<unsigned>(__LINE__));
+#endif
+            pv_ok = false;
+          }
+          if ((spin & 255) == 255 && *abort) pv_ok = false;
+        }
         if (pv_ok) {
           tc_fence_after();
-          const uint64_t dv = desc_advance(d_v, (j % kStages) * kStageBytes);
+          const uint64_t dv = desc_advance(d_v, (g % kStages) * kStageBytes);
           const uint32_t pb = tmem + kColP;
 #pragma unroll
           for (int ks = 0; ks < kNk / 16; ++ks)
             mma_ts(tmem + kColO, pb + ks * 8, desc_advance(dv, ks * 16 * 128), kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(&sh.k_empty[j % kStages]);
-          sh.pv_next = j + 1;
+          mma_commit(&sh.k_empty[g % kStages]);
+          sh.pv_next = g + 1;
         }
       }
       if (!__all_sync(0xffffffffu, pv_ok)) {
@@ -683,7 +711,7 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
     const float l_o = fin[((set ^ 1) * 2 + 0) * kTileRows + r], m_o = fin[((set ^ 1) * 2 + 1) * kTileRows + r];
     const float m_fin = fmaxf(m_ref, m_o);
     const float lrow = (l > 0.f ? l * fast_exp2(m_ref - m_fin) : 0.f) + (l_o > 0.f ? l_o * fast_exp2(m_o - m_fin) : 0.f);
-    if (ok && !mbar_wait_abortable(&sh.k_empty[(ntiles - 1) % kStages], ((ntiles - 1) / kStages) & 1, abort))
+    if (ok && !mbar_wait_abortable(&sh.k_empty[(G + ntiles - 1) % kStages], ((G + ntiles - 1) / kStages) & 1, abort, false, __LINE__))
       ok = false;
     tc_fence_after();
     if (__all_sync(0xffffffffu, ok)) {
@@ -722,7 +750,7 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
   if (warp >= 4 && (warp & 3) == 0 && lane == 0) {
     // the P.V MMAs this thread issued: all complete before TMEM is released (also after a timeout)
     mma_commit(&sh.mma_drain);
-    mbar_wait(&sh.mma_drain, 0);
+    mbar_wait(&sh.mma_drain, pass & 1);
   }
   if (!ok) {
     *abort = 1;
@@ -733,20 +761,20 @@ __device__ __forceinline__ bool run_unit(const PrefixParams& p, Shared& sh, uint
   if (*abort && warp >= 1 && warp < 4 && lane == 0) {
     // after a timeout, bulk copies of unconsumed stages may still be landing:
     // wait for them (bounded) before the shared memory is released
-    for (int t = max(0, issued - kStages); t < issued; ++t) mbar_wait(&sh.k_full[t % kStages], (t / kStages) & 1);
+    for (int t = max(G, issued - kStages); t < issued; ++t) mbar_wait(&sh.k_full[t % kStages], (t / kStages) & 1);
   }
-  // The pair's 16-bit pass decides together whether to rerun with 20-bit
-  // mantissas: each CTA sends the peer its flag word (bit 0: a partial needed
-  // more than 16 bits, bit 1: this CTA gave up on a wait), and the unit is
-  // rerun only if some partial needed it and neither CTA aborted (copies of an
-  // aborted pass may still be landing, so its barriers are not set up again).
-  if (!kWide && tid == 0)
-    st_shared_cluster_b32(mapa_shared(smem_u32(&sh.peer_need_wide), rank ^ 1u), sh.need_wide | (*abort ? 2 : 0));
+  // The pair decides together what comes next: each CTA sends the peer its flag
+  // word (kUnitWide: a partial of the 16-bit pass needed more than 16 bits;
+  // kUnitAborted: this CTA gave up on a wait).  The unit is rerun with 20-bit
+  // mantissas only if some partial needed it and neither CTA aborted; after an
+  // abort neither CTA runs another pass (its barriers' phases are unknown).
+  if (tid == 0)
+    st_shared_cluster_b32(mapa_shared(smem_u32(&sh.peer_need_wide), rank ^ 1u),
+                          (kWide ? 0 : sh.need_wide) | (*abort ? kUnitAborted : 0));
   cluster_sync();  // no CTA leaves (or starts another pass) while its peer may still write into its shared memory
-  if (kWide) return false;
-  const int flags = sh.need_wide | (*abort ? 2 : 0) | sh.peer_need_wide;
-  __syncthreads();  // every thread has read the flags before a second pass resets them
-  return flags == 1;
+  const int flags = (kWide ? 0 : sh.need_wide) | (*abort ? kUnitAborted : 0) | sh.peer_need_wide;
+  __syncthreads();  // every thread has read the flags before the next pass resets them
+  return flags;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_pair_kernel(const __grid_constant__ PrefixParams p) {
@@ -792,11 +820,138 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     tmem_alloc(&sh.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (run_unit<false>(p, sh, smem_raw, row_tile, split, b, kbegin, kend, rows_b)) {
+  if (tid == 0) init_barriers(sh);
+  if (run_unit<false>(p, sh, smem_raw, row_tile, split, b, kbegin, kend, rows_b, 0, 0) == kUnitWide) {
 #ifdef DDT_TEST_HOOKS
     if (tid == 0 && rank == 0) atomicAdd(p.status + 2, 1);  // test builds count the 20-bit reruns
 #endif
-    run_unit<true>(p, sh, smem_raw, row_tile, split, b, kbegin, kend, rows_b);
+    run_unit<true>(p, sh, smem_raw, row_tile, split, b, kbegin, kend, rows_b, (kend - kbegin + kNk - 1) / kNk, 1);
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(sh.tmem_base, kTmemCols);
+  }
+}
+
+// Fused kernel: merge the rows of one (request, row tile): the tree tail of
+// each row and the log-sum-exp merge with the request's nsplit prefix partials.
+// Rank r of the pair takes rows [64 r, 64 r + 64) of the tile, a warp every
+// 12th of them; rows of inactive nodes (ragged trees) get out = 0, lse = -inf.
+// The stage ring is idle between units and holds each warp's ancestor list.
+__device__ __noinline__ void merge_tile(const FusedParams& f, uint8_t* smem, int b, int tile, int nsplit,
+                                           int rows_b) {
+  const PrefixParams& p = f.pre;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int T = p.nodes, H = p.heads;
+  const int tile_rows = min(kTileRows, T * H - tile * kTileRows);
+  int* vis = reinterpret_cast<int*>(smem) + warp * kMaxNodes;
+  const int64_t pstride = static_cast<int64_t>(p.row_tiles) * kTileRows;
+  const MergeRowArgs a{p.q, p.scale_log2, p.o_part, p.lse_part, pstride, f.out, f.lse};
+  const int32_t* par = f.tree_parent + static_cast<int64_t>(b) * T;
+  const int32_t* tslot = f.tree_slot_idx + static_cast<int64_t>(b) * T;
+  const int i_end = min(static_cast<int>(rank) * 64 + 64, tile_rows);
+  for (int i = static_cast<int>(rank) * 64 + warp; i < i_end; i += kThreads / 32) {
+    const int r = tile * kTileRows + i, t = r / H, h = r - t * H;
+    const int64_t grow = static_cast<int64_t>(b) * T * H + r;
+    if (r >= rows_b) {
+      write_inactive_row(f.out, f.lse, grow, lane);
+      continue;
+    }
+    int n = 0;
+    if (lane == 0) {
+      int32_t st = 0;
+      n = ancestor_slots(t, T, p.pool_slots, [&](int u) { return __ldg(par + u); }, [&](int u) { return __ldg(tslot + u); },
+                         vis, &st);
+      if (st && h == 0) atomicOr(p.status, st);
+    }
+    n = __shfl_sync(0xffffffffu, n, 0);
+    __syncwarp();
+    merge_row<false>(a, grow, static_cast<int64_t>(b) * p.max_splits * pstride + r, nsplit, n,
+                     [&](int v) { return reinterpret_cast<const uint32_t*>(p.kv + static_cast<int64_t>(vis[v]) * kDqk); },
+                     lane);
+    __syncwarp();
+  }
+}
+
+// One launch per verify call.  A persistent grid of CTA pairs takes the units
+// (request b, key split, 128-row tile), tile fastest, in turn: pair k does units
+// k, k + pairs, ...  A unit is one run_unit (the 16-bit pass, rerun with 20-bit
+// mantissas where needed) writing its normalised partial; then rank 0 counts
+// the split in the workspace (release: fence, then atomic add) and the pair
+// that completes a (request, row tile) merges its rows (acquire: fence before
+// the reads, which go through L2).  Nothing waits on another pair, so no unit
+// order or residency can stall the grid.  A tile with no prefix keys (empty
+// prefix) or no active row (ragged trees) is merged, or zeroed, by its split-0
+// unit.  The merge reads the splits in order, so results do not depend on which
+// pair merges, and are the same bits as the two-kernel path's.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) verify_fused_kernel(const __grid_constant__ FusedParams f) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Shared sh;
+  const PrefixParams& p = f.pre;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (warp == 0) {
+    tmem_alloc(&sh.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) init_barriers(sh);
+  int G = 0, pass = 0;  // the CTA's steps and passes so far (barrier phases run on across units)
+  const int pairs = gridDim.x >> 1, pair = blockIdx.x >> 1;
+  for (int u = pair; u < f.units; u += pairs) {
+    const int tile = u % p.row_tiles;
+    const int split = (u / p.row_tiles) % f.splits;
+    const int b = u / (p.row_tiles * f.splits);
+    const bool first = split == 0 && tile == 0 && rank == 0 && tid == 0;  // reports the request's status bits
+    int L = __ldg(p.prefix_len + b);
+    if (L < 0 || L > p.max_prefix_len) {
+      if (first) atomicOr(p.status, kStatusBadPrefix);
+      L = L < 0 ? 0 : p.max_prefix_len;
+    }
+    int rows_b = p.rows;
+    if (p.tree_len != nullptr) {
+      int tl = __ldg(p.tree_len + b);
+      if (tl < 0 || tl > p.nodes) {
+        if (first) atomicOr(p.status, kStatusBadTreeLen);
+        tl = tl < 0 ? 0 : p.nodes;
+      }
+      rows_b = tl * p.heads;
+    }
+    const int nsplit = (L + p.chunk - 1) / p.chunk;
+    if (tile * kTileRows >= rows_b || nsplit == 0) {
+      if (split == 0) merge_tile(f, smem, b, tile, 0, rows_b);  // tree tail only, or inactive rows
+      __syncthreads();
+      continue;
+    }
+    if (split >= nsplit) continue;
+    const int kbegin = split * p.chunk, kend = min(L, kbegin + p.chunk);
+    const int ntiles = (kend - kbegin + kNk - 1) / kNk;
+    int flags = run_unit<false>(p, sh, smem_raw, tile, split, b, kbegin, kend, rows_b, G, pass);
+    G += ntiles;
+    ++pass;
+    if (flags == kUnitWide) {
+#ifdef DDT_TEST_HOOKS
+      if (tid == 0 && rank == 0) atomicAdd(p.status + 2, 1);  // test builds count the 20-bit reruns
+#endif
+      flags = run_unit<true>(p, sh, smem_raw, tile, split, b, kbegin, kend, rows_b, G, pass);
+      G += ntiles;
+      ++pass;
+    }
+    if (flags & kUnitAborted) break;  // both CTAs of the pair stop (the status word says TIMEOUT)
+    // both CTAs' partials are written (run_unit ended with a cluster barrier)
+    if (rank == 0 && tid == 0) {
+      __threadfence();
+      const int last = atomicAdd(f.arrivals + static_cast<int64_t>(b) * p.row_tiles + tile, 1) == nsplit - 1;
+      sh.last_arrival = last;
+      st_shared_cluster_b32(mapa_shared(smem_u32(&sh.last_arrival), 1u), last);
+    }
+    cluster_sync();
+    if (sh.last_arrival) {
+      __threadfence();
+      merge_tile(f, smem, b, tile, nsplit, rows_b);
+    }
+    __syncthreads();  // every thread has read last_arrival and left the ring before the next unit
   }
   if (warp == 0) {
     tc_fence_after();
@@ -806,8 +961,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 
 }  // namespace
 
+namespace {
+int g_fused_pairs[64];  // co-resident pairs per device, found once by configure_prefix
+}
+
 cudaError_t configure_prefix() {
-  return cudaFuncSetAttribute(prefix_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaError_t e = cudaFuncSetAttribute(prefix_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(verify_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess)
+    return e;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, verify_fused_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // clear it: the planner then falls back to the SM count
+    n = 0;
+  }
+  if (dev >= 0 && dev < 64) g_fused_pairs[dev] = n;
+  return cudaSuccess;
+}
+
+int fused_max_pairs() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  return g_fused_pairs[dev];
+}
+
+cudaError_t launch_fused(const FusedParams& p, int pairs, cudaStream_t stream) {
+  verify_fused_kernel<<<dim3(2 * pairs), kThreads, kSmem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prefix(const PrefixParams& p, int batch, int splits, cudaStream_t stream) {
@@ -817,3 +1003,16 @@ cudaError_t launch_prefix(const PrefixParams& p, int batch, int splits, cudaStre
 }
 
 }  // namespace ddt
+
+#ifdef DDT_TEST_HOOKS
+// Test builds only (not part of the public header).
+extern "C" __attribute__((visibility("default"))) unsigned ddtree_test_timeout_site() {
+  unsigned v = 0;
+  return cudaMemcpyFromSymbol(&v, ddt::g_timeout_site, sizeof v) == cudaSuccess ? v : 0xFFFFFFFFu;
+}
+extern "C" __attribute__((visibility("default"))) void ddtree_test_clear_timeout_site() {
+  const unsigned z = 0;
+  cudaMemcpyToSymbol(ddt::g_timeout_site, &z, sizeof z);
+}
+extern "C" __attribute__((visibility("default"))) int ddtree_test_fused_pairs() { return ddt::fused_max_pairs(); }
+#endif

@@ -85,14 +85,24 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
       : "memory");
   return ok != 0;
 }
+#ifdef DDT_TEST_HOOKS
+// Test builds: the source line of the first wait that ran out (0: none).
+__device__ unsigned int g_timeout_site;
+#endif
+
 // Bounded waits that also give up as soon as another thread of the CTA has
 // raised *abort (a volatile shared flag), so one expired wait ends them all.
+// `site` identifies the call (test builds record the first one that expires).
 __device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                    bool cluster_scope = false, uint32_t limit = DDT_WAIT_LIMIT) {
+                                                    bool cluster_scope = false, uint32_t site = 0,
+                                                    uint32_t limit = DDT_WAIT_LIMIT) {
   for (uint32_t i = 0; i < limit; ++i) {
     if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 63 && *abort) return false;
   }
+#ifdef DDT_TEST_HOOKS
+  atomicCAS(&g_timeout_site, 0u, site);
+#endif
   *abort = 1;
   return false;
 }

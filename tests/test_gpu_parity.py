@@ -208,3 +208,28 @@ def test_c5_compaction_bit_exact():
     assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
     ref_o, ref_l, _ = oracle_full("c5")
     compare(out2, lse2, ref_o, ref_l)
+
+
+# ----------------------------------------------------------------------------- fused launch vs the two phases
+
+@pytest.mark.parametrize("kw", [
+    dict(),                                                                   # tiny
+    dict(prefix=(4099,), nodes=33, heads=16, max_depth=6, max_branch=4, pool_slots=1 << 16),
+    dict(batch=3, prefix=("list", 700, 0, 2000), nodes=17, heads=20, pool_slots=1 << 16, slots="churn"),
+])
+def test_fused_launch_equals_the_two_phases(kw):
+    # ddtree_verify_attn runs one persistent kernel with the merge of each row tile done by the pair
+    # that finishes its last split; the two phase entry points run the prefix pass and the tail/merge
+    # kernel separately.  Same arithmetic, so the same bits.
+    w = wl.make_workload("tiny", **kw)
+    d = wl.to_device(w, "cuda", poison=True)
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len)
+    args = (d["q"], d["kv_pool"], d["slot_idx"], d["prefix_len"], d["tree_parent"], d["tree_slot_idx"], w.sm_scale)
+    o1, l1 = v(*args)
+    assert v.status() == 0
+    o2, l2 = v(*args, phase="prefix")
+    o2, l2 = v(*args, out=o2, lse=l2, phase="merge")
+    assert v.status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ref_o, ref_l, _ = oracle.verify_workload(w)
+    compare(o1, l1, ref_o, ref_l)
