@@ -119,16 +119,40 @@ DDT_API size_t ddtree_verify_workspace_bytes(const ddt_dims* dims);
  *                 256-byte aligned; holds the per-split partial results and the
  *                 status word.  Calls sharing a workspace must not overlap.
  *
- * Enqueues a prefix kernel (split-KV over each request's key range, all T*H rows
- * of a request contracted together on the tensor cores) and a tail kernel (tree
- * ancestors under the visibility rule, then the log-sum-exp merge of all parts).
- * Capturable in a CUDA graph.  B = 0 enqueues nothing and returns DDT_OK.
+ * The prefix part is split-KV over each request's key range, all T*H rows of a
+ * request contracted together on the tensor cores; the tree part applies the
+ * ancestor rule; a log-sum-exp merge combines them.  The call enqueues a
+ * workspace clear, the prefix pass and the tail/merge kernel (exactly
+ * ddtree_verify_prefix_phase then ddtree_verify_merge_phase; the second kernel
+ * starts as a programmatic dependent of the first).  ddtree_verify_attn_fused
+ * computes the same bits in one launch.  Capturable in a CUDA graph.  B = 0
+ * enqueues nothing and returns DDT_OK.
  */
 DDT_API int ddtree_verify_attn(const void* q, const void* kv_pool, const int32_t* slot_idx,
                        const int32_t* prefix_len, const int32_t* tree_parent,
                        const int32_t* tree_slot_idx, float sm_scale, float* out, float* lse,
                        const ddt_dims* dims, void* workspace, size_t workspace_bytes,
                        ddt_stream_t stream);
+
+/*
+ * The same computation as ddtree_verify_attn, always as one launch ("The Art of
+ * Systematic Investigation", section "Input Knowledge Required to Understand
+ * This Message", item 5, and "The Anatomy of a Kernel Investigation", section
+ * "Conclusion": the verify kernel is captured in a CUDA graph; here it is a
+ * single node besides the workspace clear).  A persistent grid of CTA pairs
+ * works through the (request, key split, 128-row tile) units; the pair that
+ * finishes the last split of a (request, row tile) merges its rows (tree tail
+ * and log-sum-exp merge), counted with an atomic in the workspace: nothing ever
+ * waits on another pair.  Same arguments, checks and results (bit for bit) as
+ * ddtree_verify_attn.  It is slower than ddtree_verify_attn's two launches (the
+ * merges run on the pairs that finish row tiles, not on every SM), so it is for
+ * callers that want the single launch.
+ */
+DDT_API int ddtree_verify_attn_fused(const void* q, const void* kv_pool, const int32_t* slot_idx,
+                                     const int32_t* prefix_len, const int32_t* tree_parent,
+                                     const int32_t* tree_slot_idx, float sm_scale, float* out, float* lse,
+                                     const ddt_dims* dims, void* workspace, size_t workspace_bytes,
+                                     ddt_stream_t stream);
 
 /*
  * Ragged trees: the same call for a batch whose requests have different node

@@ -185,6 +185,12 @@ namespace {
 
 enum Phase : int { kPhasePrefix = 1, kPhaseMerge = 2, kPhaseFused = 4 };
 
+// The fused launch's persistent grid: at most the CTA pairs that fit at once.
+int fused_pairs(const DeviceInfo& dev) {
+  const int pairs = fused_max_pairs();
+  return pairs > 0 ? pairs : (dev.sm_count >= 2 ? dev.sm_count / 2 : 1);
+}
+
 int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t* slot_idx,
                   const int32_t* prefix_len, const int32_t* tree_parent, const int32_t* tree_slot_idx,
                   const int32_t* tree_len, float sm_scale, float* out, float* lse, const ddt_dims* dims,
@@ -257,8 +263,7 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
         const int64_t units = int64_t(dims->batch) * fp.splits * plan.row_tiles;
         if (units > INT32_MAX) return DDT_ERR_DIMS;
         fp.units = static_cast<int32_t>(units);
-        int pairs = fused_max_pairs();
-        if (pairs <= 0) pairs = dev.sm_count >= 2 ? dev.sm_count / 2 : 1;
+        int pairs = fused_pairs(dev);
         if (pairs > fp.units) pairs = fp.units;
         if (launch_fused(fp, pairs, s) != cudaSuccess) return DDT_ERR_LAUNCH;
         return DDT_OK;
@@ -304,15 +309,22 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
   q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, nullptr, sm_scale, out, lse, dims, workspace, \
       workspace_bytes, stream
 
-extern "C" int ddtree_verify_attn(DDT_VERIFY_ARGS) { return verify_phases(kPhaseFused, DDT_VERIFY_PASS); }
+// Two launches (the prefix pass, then the tail/merge kernel as its programmatic
+// dependent) measured faster than the single fused launch on every
+// configuration: the merge then runs on every SM, overlapping the end of the
+// prefix pass, instead of on the pair that finishes a row tile's last split.
+extern "C" int ddtree_verify_attn(DDT_VERIFY_ARGS) {
+  return verify_phases(kPhasePrefix | kPhaseMerge, DDT_VERIFY_PASS);
+}
+extern "C" int ddtree_verify_attn_fused(DDT_VERIFY_ARGS) { return verify_phases(kPhaseFused, DDT_VERIFY_PASS); }
 extern "C" int ddtree_verify_attn_ragged(const void* q, const void* kv_pool, const int32_t* slot_idx,
                                          const int32_t* prefix_len, const int32_t* tree_parent,
                                          const int32_t* tree_slot_idx, const int32_t* tree_len, float sm_scale,
                                          float* out, float* lse, const ddt_dims* dims, void* workspace,
                                          size_t workspace_bytes, ddt_stream_t stream) {
   if (!tree_len && dims && dims->batch > 0) return DDT_ERR_NULL;
-  return verify_phases(kPhaseFused, q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, tree_len, sm_scale,
-                       out, lse, dims, workspace, workspace_bytes, stream);
+  return verify_phases(kPhasePrefix | kPhaseMerge, q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx,
+                       tree_len, sm_scale, out, lse, dims, workspace, workspace_bytes, stream);
 }
 extern "C" int ddtree_verify_prefix_phase(DDT_VERIFY_ARGS) { return verify_phases(kPhasePrefix, DDT_VERIFY_PASS); }
 extern "C" int ddtree_verify_merge_phase(DDT_VERIFY_ARGS) { return verify_phases(kPhaseMerge, DDT_VERIFY_PASS); }

@@ -159,6 +159,7 @@ struct Shared {
   uint32_t tmem_base;
   int abort;
   int last_arrival;           // fused kernel: this pair finished the last split of its (request, row tile)
+  int unit[2];                // fused kernel: the units the pair claimed, by claim parity
   int need_wide;              // 16-bit pass: a partial of this CTA needed more than 16-bit mantissas
   int peer_need_wide;         // the peer CTA's flag word (stored remotely at the end of the 16-bit pass)
 };
@@ -837,46 +838,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
 // each row and the log-sum-exp merge with the request's nsplit prefix partials.
 // Rank r of the pair takes rows [64 r, 64 r + 64) of the tile, a warp every
 // 12th of them; rows of inactive nodes (ragged trees) get out = 0, lse = -inf.
-// The stage ring is idle between units and holds each warp's ancestor list.
+// The stage ring is idle between units: it holds the request's parent and slot
+// arrays, all its tree rows (T x 1152 B) and, per node of this CTA's rows, the
+// list of its visible tree nodes, so a row's tail reads shared memory only.
 __device__ __noinline__ void merge_tile(const FusedParams& f, uint8_t* smem, int b, int tile, int nsplit,
-                                           int rows_b) {
+                                        int rows_b) {
   const PrefixParams& p = f.pre;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const int T = p.nodes, H = p.heads;
   const int tile_rows = min(kTileRows, T * H - tile * kTileRows);
-  int* vis = reinterpret_cast<int*>(smem) + warp * kMaxNodes;
-  const int64_t pstride = static_cast<int64_t>(p.row_tiles) * kTileRows;
-  const MergeRowArgs a{p.q, p.scale_log2, p.o_part, p.lse_part, pstride, f.out, f.lse};
+  const int i_beg = static_cast<int>(rank) * 64, i_end = min(i_beg + 64, tile_rows);
+  if (i_beg >= i_end) return;
+  const int r_beg = tile * kTileRows + i_beg, r_end = tile * kTileRows + i_end;  // rows of the request
+  const int n_beg = r_beg / H, n_cnt = (r_end - 1) / H - n_beg + 1;              // their nodes (<= 64)
+  uint8_t* rows_sh = smem;                                                       // [T][1152]
+  int* par_sh = reinterpret_cast<int*>(smem + kMaxNodes * kRowBytes);            // [T]
+  int* tslot_sh = par_sh + kMaxNodes;                                            // [T]
+  int* nvis_sh = tslot_sh + kMaxNodes;                                           // [n_cnt]
+  int* vis_sh = nvis_sh + 64;                                                    // [n_cnt][T] node lists
+  static_assert(kMaxNodes * kRowBytes + (3 * kMaxNodes + 64 + 64 * kMaxNodes) * 4 <= kStages * kStageBytes,
+                "the merge's staging fits in the stage ring");
   const int32_t* par = f.tree_parent + static_cast<int64_t>(b) * T;
   const int32_t* tslot = f.tree_slot_idx + static_cast<int64_t>(b) * T;
-  const int i_end = min(static_cast<int>(rank) * 64 + 64, tile_rows);
-  for (int i = static_cast<int>(rank) * 64 + warp; i < i_end; i += kThreads / 32) {
-    const int r = tile * kTileRows + i, t = r / H, h = r - t * H;
+  for (int u = tid; u < T; u += kThreads) {
+    par_sh[u] = __ldg(par + u);
+    tslot_sh[u] = __ldg(tslot + u);
+  }
+  __syncthreads();
+  // the request's tree rows (rows of out-of-pool slots are never read: the walk leaves them out)
+  for (int i = tid; i < T * kChunks; i += kThreads) {
+    const int u = i / kChunks, c = i - u * kChunks;
+    const int32_t slot = tslot_sh[u];
+    if (slot >= 0 && static_cast<int64_t>(slot) < p.pool_slots)
+      reinterpret_cast<uint4*>(rows_sh + u * kRowBytes)[c] =
+          __ldg(reinterpret_cast<const uint4*>(p.kv + static_cast<int64_t>(slot) * kDqk) + c);
+  }
+  // one thread per node: its visible nodes (itself, its parent, ..., the root)
+  if (tid < n_cnt) {
+    const int t = n_beg + tid;
+    int32_t st = 0;
+    int* list = vis_sh + tid * kMaxNodes;
+    int n = 0, u = t;
+    for (int guard = 0; u >= 0 && guard < T; ++guard) {
+      const int32_t slot = tslot_sh[u];
+      if (slot >= 0 && static_cast<int64_t>(slot) < p.pool_slots)
+        list[n++] = u;
+      else
+        st |= kStatusBadSlot;
+      const int pu = par_sh[u];
+      const bool ok = (u == 0) ? (pu == -1) : (pu >= 0 && pu < u);
+      if (!ok) {
+        st |= kStatusBadParent;
+        break;
+      }
+      u = pu;
+    }
+    nvis_sh[tid] = n;
+    if (st && t * H < rows_b) atomicOr(p.status, st);
+  }
+  __syncthreads();
+  const int64_t pstride = static_cast<int64_t>(p.row_tiles) * kTileRows;
+  const MergeRowArgs a{p.q, p.scale_log2, p.o_part, p.lse_part, pstride, f.out, f.lse};
+  for (int r = r_beg + warp; r < r_end; r += kThreads / 32) {
+    const int t = r / H;
     const int64_t grow = static_cast<int64_t>(b) * T * H + r;
     if (r >= rows_b) {
       write_inactive_row(f.out, f.lse, grow, lane);
       continue;
     }
-    int n = 0;
-    if (lane == 0) {
-      int32_t st = 0;
-      n = ancestor_slots(t, T, p.pool_slots, [&](int u) { return __ldg(par + u); }, [&](int u) { return __ldg(tslot + u); },
-                         vis, &st);
-      if (st && h == 0) atomicOr(p.status, st);
-    }
-    n = __shfl_sync(0xffffffffu, n, 0);
-    __syncwarp();
-    merge_row<false>(a, grow, static_cast<int64_t>(b) * p.max_splits * pstride + r, nsplit, n,
-                     [&](int v) { return reinterpret_cast<const uint32_t*>(p.kv + static_cast<int64_t>(vis[v]) * kDqk); },
-                     lane);
-    __syncwarp();
+    const int* list = vis_sh + (t - n_beg) * kMaxNodes;
+    merge_row<false>(a, grow, static_cast<int64_t>(b) * p.max_splits * pstride + r, nsplit, nvis_sh[t - n_beg],
+                     [&](int v) { return reinterpret_cast<const uint32_t*>(rows_sh + list[v] * kRowBytes); }, lane);
   }
 }
 
-// One launch per verify call.  A persistent grid of CTA pairs takes the units
-// (request b, key split, 128-row tile), tile fastest, in turn: pair k does units
-// k, k + pairs, ...  A unit is one run_unit (the 16-bit pass, rerun with 20-bit
+// One launch per verify call.  A persistent grid of CTA pairs claims the units
+// (request b, key split, 128-row tile), tile fastest, from a counter, so pairs
+// whose units end early (or are empty: splits past a shorter prefix) take more.
+// A unit is one run_unit (the 16-bit pass, rerun with 20-bit
 // mantissas where needed) writing its normalised partial; then rank 0 counts
 // the split in the workspace (release: fence, then atomic add) and the pair
 // that completes a (request, row tile) merges its rows (acquire: fence before
@@ -898,8 +938,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) verify_
   }
   if (tid == 0) init_barriers(sh);
   int G = 0, pass = 0;  // the CTA's steps and passes so far (barrier phases run on across units)
-  const int pairs = gridDim.x >> 1, pair = blockIdx.x >> 1;
-  for (int u = pair; u < f.units; u += pairs) {
+  for (int it = 0;; ++it) {
+    // Rank 0 claims the next unit for the pair (a counter in the status words,
+    // zero at launch) and hands it to rank 1 through its shared memory.  Claims
+    // alternate between two slots: a slot is rewritten two claims later, past a
+    // cluster barrier that every thread reaches only after reading it.
+    if (rank == 0 && tid == 0) {
+      const int claimed = atomicAdd(p.status + 3, 1);
+      sh.unit[it & 1] = claimed;
+      st_shared_cluster_b32(mapa_shared(smem_u32(&sh.unit[it & 1]), 1u), claimed);
+    }
+    cluster_sync();
+    const int u = sh.unit[it & 1];
+    if (u >= f.units) break;
+    // units in request, key split, row tile order (tile fastest): the pairs at work at one time
+    // share one or two key ranges, whose rows stay in L2
     const int tile = u % p.row_tiles;
     const int split = (u / p.row_tiles) % f.splits;
     const int b = u / (p.row_tiles * f.splits);

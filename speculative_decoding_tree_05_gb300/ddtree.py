@@ -24,7 +24,8 @@ STATUS_BAD_PREFIX = 4
 STATUS_TIMEOUT = 8
 STATUS_BAD_TREE_LEN = 16
 
-EXPORTS = ("ddtree_verify_workspace_bytes", "ddtree_verify_attn", "ddtree_verify_attn_ragged",
+EXPORTS = ("ddtree_verify_workspace_bytes", "ddtree_verify_attn", "ddtree_verify_attn_fused",
+           "ddtree_verify_attn_ragged",
            "ddtree_verify_prefix_phase",
            "ddtree_verify_merge_phase", "ddtree_verify_attn_static_scratch", "ddtree_kv_compact",
            "ddtree_kv_compact_check",
@@ -57,7 +58,10 @@ def load(path: str):
     vp, i32p = ctypes.c_void_p, ctypes.c_void_p
     L.ddtree_verify_workspace_bytes.restype = ctypes.c_size_t
     L.ddtree_verify_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
-    for fn in ("ddtree_verify_attn", "ddtree_verify_prefix_phase", "ddtree_verify_merge_phase"):
+    for fn in ("ddtree_verify_attn", "ddtree_verify_attn_fused", "ddtree_verify_prefix_phase",
+               "ddtree_verify_merge_phase"):
+        if not hasattr(L, fn):   # builds that predate an entry point
+            continue
         f = getattr(L, fn)
         f.restype = ctypes.c_int
         f.argtypes = [vp, vp, i32p, i32p, i32p, i32p, ctypes.c_float, vp, vp, ctypes.POINTER(Dims), vp,
@@ -140,7 +144,8 @@ class Verifier:
 
     def __call__(self, q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out=None,
                  lse=None, stream=None, phase="all", tree_len=None):
-        """phase: "all" (ddtree_verify_attn), "prefix" or "merge" (the two halves of it).
+        """phase: "all" (ddtree_verify_attn), "fused" (ddtree_verify_attn_fused: always one launch),
+        "prefix" or "merge" (the two-launch path's halves).
 
         tree_len: optional int32 [B] CUDA tensor of active nodes per request
         (ddtree_verify_attn_ragged; phase must be "all").
@@ -160,7 +165,7 @@ class Verifier:
                                                  _ptr(self.workspace), self.workspace.numel(), _stream(stream))
             _check(rc, "ddtree_verify_attn_ragged")
             return out, lse
-        fn = {"all": "ddtree_verify_attn", "prefix": "ddtree_verify_prefix_phase",
+        fn = {"all": "ddtree_verify_attn", "fused": "ddtree_verify_attn_fused", "prefix": "ddtree_verify_prefix_phase",
               "merge": "ddtree_verify_merge_phase"}[phase]
         rc = getattr(self.lib, fn)(_ptr(q), _ptr(kv_pool), _ptr(slot_idx), _ptr(prefix_len), _ptr(tree_parent),
                                 _ptr(tree_slot_idx), float(sm_scale), _ptr(out), _ptr(lse),

@@ -218,18 +218,35 @@ def test_c5_compaction_bit_exact():
     dict(batch=3, prefix=("list", 700, 0, 2000), nodes=17, heads=20, pool_slots=1 << 16, slots="churn"),
 ])
 def test_fused_launch_equals_the_two_phases(kw):
-    # ddtree_verify_attn runs one persistent kernel with the merge of each row tile done by the pair
-    # that finishes its last split; the two phase entry points run the prefix pass and the tail/merge
-    # kernel separately.  Same arithmetic, so the same bits.
+    # ddtree_verify_attn_fused runs one persistent kernel with the merge of each row tile done by the
+    # pair that finishes its last split; the two phase entry points run the prefix pass and the
+    # tail/merge kernel separately.  Same arithmetic, so the same bits.
     w = wl.make_workload("tiny", **kw)
     d = wl.to_device(w, "cuda", poison=True)
     v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len)
     args = (d["q"], d["kv_pool"], d["slot_idx"], d["prefix_len"], d["tree_parent"], d["tree_slot_idx"], w.sm_scale)
-    o1, l1 = v(*args)
+    o1, l1 = v(*args, phase="fused")
     assert v.status() == 0
     o2, l2 = v(*args, phase="prefix")
     o2, l2 = v(*args, out=o2, lse=l2, phase="merge")
     assert v.status() == 0
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     ref_o, ref_l, _ = oracle.verify_workload(w)
+    compare(o1, l1, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name", ["c3", "c5"])
+def test_fused_launch_full_size(name):
+    # multi-wave configurations of the single fused launch: every element against the oracle, and the
+    # same bits as the two-launch path
+    w = wl.make_workload(name)
+    d = wl.to_device(w, "cuda", poison=True)
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len)
+    args = (d["q"], d["kv_pool"], d["slot_idx"], d["prefix_len"], d["tree_parent"], d["tree_slot_idx"], w.sm_scale)
+    o1, l1 = v(*args, phase="fused")
+    assert v.status() == 0
+    o2, l2 = v(*args, phase="prefix")
+    o2, l2 = v(*args, out=o2, lse=l2, phase="merge")
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ref_o, ref_l, _ = oracle_full(name)
     compare(o1, l1, ref_o, ref_l)
