@@ -11,7 +11,9 @@ Contents
   verify_attn_ragged(...) the same for requests with tree_len[b] <= T active nodes each
   tree_visibility(parent) the tree part of the visibility mask, via the C oracle
   kv_compact(...)         row-copy compaction via the C oracle
+  verify_sparse(...)      fp64 sparse-index variant: each node lists its key slots (-1 = none)
   brute_force(...)        NumPy fp64 re-derivation for tiny inputs (independent code path)
+  brute_force_sparse(...) the same for the sparse-index variant
 
 The definition both follow: every tree node sees the whole prefix and, among the
 tree nodes, its ancestors and itself ("The Art of Systematic Investigation",
@@ -65,6 +67,9 @@ def load(path: str | None = None):
                                        ctypes.c_double, p, ctypes.c_int64, p, p]
     lib.oracle_tree_visibility.restype = ctypes.c_int
     lib.oracle_tree_visibility.argtypes = [p, ctypes.c_int, p]
+    lib.oracle_verify_sparse.restype = ctypes.c_int
+    lib.oracle_verify_sparse.argtypes = [p, p, ctypes.c_int64, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_double, p, p]
     lib.oracle_kv_compact.restype = ctypes.c_int
     lib.oracle_kv_compact.argtypes = [p, p, ctypes.c_int64, p, ctypes.c_int64, p, p, ctypes.c_int,
                                       ctypes.c_int, p]
@@ -151,6 +156,26 @@ def verify_workload(w, rows=None, lib=None):
     return verify_attn(w.q_bits, pool, si, w.prefix_len, w.tree_parent, ts, w.sm_scale, rows=rows, lib=lib)
 
 
+def verify_sparse(q_bits, pool_bits, indices, sm_scale, lib=None):
+    """fp64 sparse-index verify attention.
+
+    q_bits uint16 [B,T,H,Dqk], pool_bits uint16 [N,Dqk], indices int32 [B,T,topk] (-1 = no key).
+    Returns (out fp64 [B,T,H,Dv], lse fp64 [B,T,H], status bits).
+    """
+    lib = lib or load()
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    pool = np.ascontiguousarray(pool_bits, dtype=np.uint16)
+    B, T, H, dqk = q.shape
+    dv = dqk - 64
+    idx = np.ascontiguousarray(indices, dtype=np.int32).reshape(B, T, -1)
+    topk = idx.shape[2]
+    out = np.zeros((B, T, H, dv), dtype=np.float64)
+    lse = np.zeros((B, T, H), dtype=np.float64)
+    st = lib.oracle_verify_sparse(_ptr(q), _ptr(pool), pool.shape[0], _ptr(idx), topk, B, T, H, dqk, dv,
+                                  float(sm_scale), _ptr(out), _ptr(lse))
+    return out, lse, st
+
+
 def tree_visibility(parent) -> tuple:
     lib = load()
     p = np.ascontiguousarray(parent, dtype=np.int32)
@@ -219,4 +244,26 @@ def brute_force(q_bits, pool_bits, slot_idx, prefix_len, tree_parent, tree_slot_
             w = np.exp(scores - lse_bt[:, None])
             out[b, t] = w @ k[:, :dv]
             lse[b, t] = lse_bt
+    return out, lse
+
+
+def brute_force_sparse(q_bits, pool_bits, indices, sm_scale):
+    """NumPy fp64 sparse-index attention for tiny, valid inputs (every listed value is -1 or a pool row):
+    dense scores over the listed rows, logaddexp reduction."""
+    q = _bf16(q_bits)
+    pool = _bf16(pool_bits)
+    B, T, H, dqk = q.shape
+    dv = dqk - 64
+    idx = np.asarray(indices).reshape(B, T, -1)
+    out = np.zeros((B, T, H, dv))
+    lse = np.full((B, T, H), -np.inf)
+    for b in range(B):
+        for t in range(T):
+            keys = pool[[int(s) for s in idx[b, t] if s != -1]]
+            if len(keys) == 0:
+                continue
+            scores = (q[b, t] @ keys.T) * sm_scale
+            l = np.logaddexp.reduce(scores, axis=1)
+            out[b, t] = np.exp(scores - l[:, None]) @ keys[:, :dv]
+            lse[b, t] = l
     return out, lse

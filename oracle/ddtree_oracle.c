@@ -210,3 +210,65 @@ int oracle_kv_compact(const uint16_t* src, uint16_t* dst, int64_t pool_slots, co
   }
   return status;
 }
+
+/*
+ * Sparse-index variant ("The Architecture Detective: Uncovering FlashMLA's
+ * Potential for Blackwell DDTree Verification", sections "The Message in Full"
+ * and "The Discovery: FlashMLA's Hidden Capabilities": a sparse attention call
+ * takes, per query, a fixed-length list of key indices in which -1 marks an
+ * invalid entry).  Here every query node lists its own keys: node (b, t) owns
+ * indices[(b*T + t)*topk .. +topk); all H heads of the node attend to the rows
+ * pool[slot] for the listed slots != -1.  A slot listed twice counts twice.
+ * A listed value outside [0, pool_slots) other than -1 is left out and
+ * reported with ORACLE_BAD_SLOT.  A node with no key gets lse = -inf, out = 0.
+ *   s_i   = sm_scale * q . pool[slot_i][0:d_qk]               (fp64)
+ *   lse   = ln sum_i exp(s_i),  out_e = sum_i exp(s_i - lse) * pool[slot_i][e]
+ */
+int oracle_verify_sparse(const uint16_t* q, const uint16_t* pool, int64_t pool_slots, const int32_t* indices,
+                         int topk, int B, int T, int H, int d_qk, int d_v, double sm_scale, double* out,
+                         double* lse) {
+  if (B < 0 || T < 1 || H < 1 || topk < 0 || d_v > d_qk || d_v < 1) return ORACLE_BAD_ARGS;
+  int flags = 0;
+  for (int64_t i = 0; i < (int64_t)B * T * topk; ++i)
+    if (indices[i] != -1 && (indices[i] < 0 || (int64_t)indices[i] >= pool_slots)) flags |= ORACLE_BAD_SLOT;
+  const int64_t n_rows = (int64_t)B * T * H;
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t row = 0; row < n_rows; ++row) {
+    const int32_t* list = indices + (row / H) * topk;
+    const uint16_t* query = q + row * (int64_t)d_qk;
+    double* score = (double*)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1));
+    unsigned char* listed = (unsigned char*)malloc((size_t)(topk > 0 ? topk : 1));
+    double best = -INFINITY;
+    for (int k = 0; k < topk; ++k) {
+      const int64_t slot = list[k];
+      listed[k] = slot >= 0 && slot < pool_slots;
+      if (!listed[k]) continue;
+      const uint16_t* key = pool + slot * d_qk;
+      double acc = 0.0;
+      for (int c = 0; c < d_qk; ++c) acc += bf16_value(query[c]) * bf16_value(key[c]);
+      score[k] = sm_scale * acc;
+      if (score[k] > best) best = score[k];
+    }
+    double* orow = out + row * (int64_t)d_v;
+    for (int c = 0; c < d_v; ++c) orow[c] = 0.0;
+    if (best == -INFINITY) {
+      lse[row] = -INFINITY;
+    } else {
+      double total = 0.0;
+      for (int i = 0; i < topk; ++i)
+        if (listed[i]) total += exp(score[i] - best);
+      const double log_norm = best + log(total);
+      lse[row] = log_norm;
+      for (int n = 0; n < topk; ++n) {
+        if (!listed[n]) continue;
+        const double weight = exp(score[n] - log_norm);
+        const uint16_t* val = pool + (int64_t)list[n] * d_qk;
+        for (int c = 0; c < d_v; ++c) orow[c] += weight * bf16_value(val[c]);
+      }
+    }
+    free(listed);
+    free(score);
+  }
+  return flags;
+}

@@ -6,7 +6,10 @@ in fp64 for the cases that reduce to textbook attention (single node = decode,
 chain = causal, star), closed forms (identical keys, a dominant key, a sparse
 worked example), invariants (inclusion-exclusion of softmax normalisers, joint
 permutation of pool rows and slot indices, compaction) and an independently
-written NumPy brute force.  A mutation test plants plausible mistakes in copies
+written NumPy brute force.  The sparse-index variant is pinned against the
+dense oracle (lists naming each node's visible keys), against closed forms
+(-1 padding and list order change nothing; listing every key twice adds ln 2 to
+the lse; an empty list gives -inf) and against its own NumPy brute force.  A mutation test plants plausible mistakes in copies
 of the oracle's C source and checks that the pins catch every one of them.
 """
 import json
@@ -246,10 +249,94 @@ def pin_bruteforce(lib):
         np.testing.assert_allclose(lse, bl, rtol=0, atol=1e-12)
 
 
+# ----------------------------------------------------------------------------- sparse-index variant
+
+def sparse_lists(c, extra=0, seed=0):
+    """Index lists that spell out each node's visible set: its request's prefix slots, then the slots of
+    the node and its ancestors (found by descent in the NumPy reading, not by the C oracle's walk),
+    padded with `extra` -1 entries; all lists are cut to one length with -1."""
+    B, T = c["tree_parent"].shape
+    lists = []
+    for b in range(B):
+        L = int(c["prefix_len"][b])
+        anc = oracle._ancestors_by_descent(list(c["tree_parent"][b]))
+        for t in range(T):
+            lists.append(list(c["slot_idx"][b, :L]) + [int(c["tree_slot_idx"][b, u]) for u in sorted(anc[t])]
+                         + [-1] * extra)
+    topk = max(len(x) for x in lists)
+    return np.asarray([x + [-1] * (topk - len(x)) for x in lists], np.int32).reshape(B, T, topk)
+
+
+def pin_sparse_equals_dense(lib):
+    # a list that names exactly a node's visible keys is dense verify attention
+    for seed, T, H, L in ((41, 5, 2, (7, 3)), (42, 9, 3, (0, 12))):
+        c = case(seed, T=T, H=H, L=L)
+        o_d, l_d, st = run(c, lib)
+        assert st == 0
+        o_s, l_s, st_s = oracle.verify_sparse(c["q_bits"], c["pool_bits"], sparse_lists(c, extra=3),
+                                              c["sm_scale"], lib=lib)
+        assert st_s == 0
+        np.testing.assert_allclose(o_s, o_d, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l_s, l_d, rtol=0, atol=1e-12)
+
+
+def pin_sparse_padding_order_duplicates(lib):
+    rng = np.random.Generator(np.random.PCG64(43))
+    c = case(43, T=4, H=3, L=(11,), N=60)
+    idx = rng.integers(0, 60, size=(1, 4, 9)).astype(np.int32)
+    o, l, _ = oracle.verify_sparse(c["q_bits"], c["pool_bits"], idx, c["sm_scale"], lib=lib)
+    # -1 entries anywhere and any order: the same attention
+    padded = np.concatenate([idx, np.full((1, 4, 5), -1, np.int32)], axis=2)
+    shuffled = np.stack([np.stack([rng.permutation(padded[0, t]) for t in range(4)])])
+    o2, l2, st = oracle.verify_sparse(c["q_bits"], c["pool_bits"], shuffled, c["sm_scale"], lib=lib)
+    assert st == 0
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l, rtol=0, atol=1e-12)
+    # every key listed twice: each weight doubles, so lse gains ln 2 and out is unchanged
+    o3, l3, _ = oracle.verify_sparse(c["q_bits"], c["pool_bits"], np.concatenate([idx, idx], axis=2),
+                                     c["sm_scale"], lib=lib)
+    np.testing.assert_allclose(o3, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l3, l + math.log(2.0), rtol=0, atol=1e-12)
+
+
+def pin_sparse_empty_list(lib):
+    c = case(44, T=3, H=2, L=(5,), N=40)
+    idx = np.asarray([[[3, 7, -1], [-1, -1, -1], [9, -1, 9]]], np.int32)
+    o, l, st = oracle.verify_sparse(c["q_bits"], c["pool_bits"], idx, c["sm_scale"], lib=lib)
+    assert st == 0
+    assert np.all(l[0, 1] == -np.inf) and np.all(o[0, 1] == 0.0)
+    assert np.isfinite(l[0, 0]).all() and np.isfinite(l[0, 2]).all()
+    # a single (twice-listed) key: out is that key's value row
+    np.testing.assert_allclose(o[0, 2], np.broadcast_to(wl.bf16_bits_to_f32(c["pool_bits"][9, :DV]), (2, DV)),
+                               rtol=0, atol=1e-12)
+
+
+def pin_sparse_bruteforce(lib):
+    rng = np.random.Generator(np.random.PCG64(45))
+    c = case(45, T=6, H=3, L=(4, 2), N=70)
+    idx = rng.integers(-1, 70, size=(2, 6, 13)).astype(np.int32)
+    o, l, st = oracle.verify_sparse(c["q_bits"], c["pool_bits"], idx, c["sm_scale"], lib=lib)
+    bo, bl = oracle.brute_force_sparse(c["q_bits"], c["pool_bits"], idx, c["sm_scale"])
+    assert st == 0
+    np.testing.assert_allclose(o, bo, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, bl, rtol=0, atol=1e-12)
+
+
+def test_sparse_bad_slot_is_left_out_and_flagged():
+    c = case(46, T=2, H=2, L=(3,), N=30)
+    good = np.asarray([[[4, 5, -1], [6, -1, -1]]], np.int32)
+    bad = np.asarray([[[4, 5, 30], [6, -7, -1]]], np.int32)
+    o1, l1, s1 = oracle.verify_sparse(c["q_bits"], c["pool_bits"], good, c["sm_scale"])
+    o2, l2, s2 = oracle.verify_sparse(c["q_bits"], c["pool_bits"], bad, c["sm_scale"])
+    assert s1 == 0 and s2 & oracle.BAD_SLOT
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
 INDEPENDENT_PINS = [pin_golden_visibility, pin_single_node_is_decode, pin_chain_is_causal,
                     pin_prefix_free_chain_is_causal, pin_star_tree, pin_identical_keys, pin_dominant_key,
-                    pin_worked_example, pin_inclusion_exclusion, pin_joint_permutation]
-ALL_PINS = INDEPENDENT_PINS + [pin_bruteforce]
+                    pin_worked_example, pin_inclusion_exclusion, pin_joint_permutation,
+                    pin_sparse_equals_dense, pin_sparse_padding_order_duplicates, pin_sparse_empty_list]
+ALL_PINS = INDEPENDENT_PINS + [pin_bruteforce, pin_sparse_bruteforce]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -324,6 +411,12 @@ MUTATIONS = {
     "tree key of the query node": (": tree_slot_idx[(int64_t)b * T + (j - L)];", ": tree_slot_idx[(int64_t)b * T + t];"),
     "neighbouring head's query": ("const uint16_t* qrow = q + row * d_qk;", "const uint16_t* qrow = q + (row ^ 1) * d_qk;"),
     "bad parent not reported": ("status |= ORACLE_BAD_PARENT;", "status |= 0;"),
+    "sparse: last listed key dropped": ("for (int k = 0; k < topk; ++k) {", "for (int k = 0; k + 1 < topk; ++k) {"),
+    "sparse: -1 read as slot 0": ("const int64_t slot = list[k];", "const int64_t slot = list[k] == -1 ? 0 : list[k];"),
+    "sparse: heads share the node's first query": ("const uint16_t* query = q + row * (int64_t)d_qk;",
+                                                   "const uint16_t* query = q + (row - row % H) * (int64_t)d_qk;"),
+    "sparse: weights not normalised": ("const double weight = exp(score[n] - log_norm);",
+                                       "const double weight = exp(score[n] - best);"),
 }
 
 
