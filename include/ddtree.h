@@ -67,7 +67,7 @@ typedef struct CUstream_st* ddt_stream_t;
 
 /*
  * Sizes of one call.  Fixed by the library: D_qk = 576, D_v = 512.
- *   batch          B >= 0 requests
+ *   batch          B in [0, 65535] requests
  *   num_nodes      T in [1, 128] tree nodes per request (node 0 is the root)
  *   num_heads      H in [1, 1024] query heads (all share the single latent KV head)
  *   pool_slots     N >= 1 rows in the KV pool
@@ -198,6 +198,31 @@ DDT_API int ddtree_verify_merge_phase(const void* q, const void* kv_pool, const 
                               const int32_t* tree_slot_idx, float sm_scale, float* out, float* lse,
                               const ddt_dims* dims, void* workspace, size_t workspace_bytes,
                               ddt_stream_t stream);
+
+/*
+ * Sparse-index variant ("The Architecture Detective: Uncovering FlashMLA's
+ * Potential for Blackwell DDTree Verification", sections "The Message in Full"
+ * and "The Discovery: FlashMLA's Hidden Capabilities": the sparse attention
+ * call takes a fixed-length list of key indices per query, -1 marking an
+ * invalid entry; the pages set it aside for this workload because every list
+ * would have to name the whole prefix).  Each tree node lists its own keys:
+ *   indices   int32 [B, T, topk] device, topk = dims->max_prefix_len; node (b, t)
+ *             attends, for all its H heads, to the rows kv_pool[indices[b][t][i]]
+ *             with indices[b][t][i] != -1.  A slot listed twice counts twice.
+ *             Other values outside [0, pool_slots) are left out and set
+ *             DDT_STATUS_BAD_SLOT.  A node with no key gets out = 0, lse = -inf.
+ *   q, out, lse as in ddtree_verify_attn ([B, T, H, ...]); dims->batch = B,
+ *   num_nodes = T, num_heads = H, pool_slots = N, max_prefix_len = topk
+ *   (slot_stride and prefix_len_sum are ignored); B * T <= 65535.
+ *   workspace >= ddtree_verify_sparse_workspace_bytes(dims).
+ * There is no tree part: the lists are the whole visible set.  The work is
+ * the prefix pass over each node's list (the node's H heads are the rows of
+ * the contraction) and the log-sum-exp merge of its key splits.
+ */
+DDT_API size_t ddtree_verify_sparse_workspace_bytes(const ddt_dims* dims);
+DDT_API int ddtree_verify_attn_sparse(const void* q, const void* kv_pool, const int32_t* indices, float sm_scale,
+                                      float* out, float* lse, const ddt_dims* dims, void* workspace,
+                                      size_t workspace_bytes, ddt_stream_t stream);
 
 /*
  * KV compaction (defragmentation) of each request's prefix rows

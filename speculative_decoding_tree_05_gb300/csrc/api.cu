@@ -52,7 +52,8 @@ struct Plan {
 
 int check_dims(const ddt_dims* d) {
   if (!d) return DDT_ERR_NULL;
-  if (d->batch < 0 || d->num_nodes < 1 || d->num_nodes > kMaxNodes || d->num_heads < 1 || d->num_heads > 1024 ||
+  if (d->batch < 0 || d->batch > 65535 || d->num_nodes < 1 || d->num_nodes > kMaxNodes || d->num_heads < 1 ||
+      d->num_heads > 1024 ||
       d->pool_slots < 1 || d->pool_slots > (int64_t(1) << 31) || d->max_prefix_len < 0 ||
       d->slot_stride < d->max_prefix_len || d->slot_stride < 0)
     return DDT_ERR_DIMS;
@@ -191,15 +192,33 @@ int fused_pairs(const DeviceInfo& dev) {
   return pairs > 0 ? pairs : (dev.sm_count >= 2 ? dev.sm_count / 2 : 1);
 }
 
+// The sparse-index call as the dense machinery sees it: each (request, node)
+// is a request of one node whose key list is its prefix (topk =
+// max_prefix_len entries, every list full length, -1 = no key).  Returns
+// DDT_ERR_DIMS when the flattened batch is too large.
+int sparse_as_dense(const ddt_dims* d, ddt_dims* e) {
+  int rc = check_dims(d);
+  if (rc != DDT_OK) return rc;
+  const int64_t batch = int64_t(d->batch) * d->num_nodes;
+  if (batch > 65535) return DDT_ERR_DIMS;
+  *e = *d;
+  e->batch = static_cast<int32_t>(batch);
+  e->num_nodes = 1;
+  e->slot_stride = d->max_prefix_len;
+  const int64_t keys = batch * d->max_prefix_len;
+  e->prefix_len_sum = keys <= INT32_MAX ? static_cast<int32_t>(keys) : 0;
+  return DDT_OK;
+}
+
 int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t* slot_idx,
                   const int32_t* prefix_len, const int32_t* tree_parent, const int32_t* tree_slot_idx,
                   const int32_t* tree_len, float sm_scale, float* out, float* lse, const ddt_dims* dims,
-                  void* workspace, size_t workspace_bytes, ddt_stream_t stream) {
+                  void* workspace, size_t workspace_bytes, ddt_stream_t stream, bool sparse = false) {
   int rc = check_dims(dims);
   if (rc != DDT_OK) return rc;
   if (dims->batch == 0) return DDT_OK;
-  if (!q || !kv_pool || !prefix_len || !tree_parent || !tree_slot_idx || !out || !lse || !workspace ||
-      (!slot_idx && dims->max_prefix_len > 0))
+  if (!q || !kv_pool || !out || !lse || !workspace || (!slot_idx && dims->max_prefix_len > 0) ||
+      (!sparse && (!prefix_len || !tree_parent || !tree_slot_idx)))
     return DDT_ERR_NULL;
   if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(workspace, 256) || !aligned(slot_idx, 4) || !aligned(prefix_len, 4) ||
@@ -239,6 +258,7 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
       pp.prefix_len = prefix_len;
       pp.pool_slots = dims->pool_slots;
       pp.slot_stride = dims->slot_stride;
+      pp.sparse = sparse ? 1 : 0;
       pp.rows = plan.rows;
       pp.heads = dims->num_heads;
       pp.nodes = dims->num_nodes;
@@ -276,6 +296,7 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
     tp.q = static_cast<const uint16_t*>(q);
     tp.kv = static_cast<const uint16_t*>(kv_pool);
     tp.prefix_len = prefix_len;
+    tp.no_tail = sparse ? 1 : 0;
     tp.tree_parent = tree_parent;
     tp.tree_slot_idx = tree_slot_idx;
     tp.pool_slots = dims->pool_slots;
@@ -327,6 +348,23 @@ extern "C" int ddtree_verify_attn_ragged(const void* q, const void* kv_pool, con
                        tree_len, sm_scale, out, lse, dims, workspace, workspace_bytes, stream);
 }
 extern "C" int ddtree_verify_prefix_phase(DDT_VERIFY_ARGS) { return verify_phases(kPhasePrefix, DDT_VERIFY_PASS); }
+
+extern "C" size_t ddtree_verify_sparse_workspace_bytes(const ddt_dims* dims) {
+  ddt_dims e;
+  if (sparse_as_dense(dims, &e) != DDT_OK) return 0;
+  return ddtree_verify_workspace_bytes(&e);
+}
+
+extern "C" int ddtree_verify_attn_sparse(const void* q, const void* kv_pool, const int32_t* indices, float sm_scale,
+                                         float* out, float* lse, const ddt_dims* dims, void* workspace,
+                                         size_t workspace_bytes, ddt_stream_t stream) {
+  if (!dims) return DDT_ERR_NULL;
+  ddt_dims e;
+  const int rc = sparse_as_dense(dims, &e);
+  if (rc != DDT_OK) return rc;
+  return verify_phases(kPhasePrefix | kPhaseMerge, q, kv_pool, indices, nullptr, nullptr, nullptr, nullptr, sm_scale,
+                       out, lse, &e, workspace, workspace_bytes, stream, true);
+}
 extern "C" int ddtree_verify_merge_phase(DDT_VERIFY_ARGS) { return verify_phases(kPhaseMerge, DDT_VERIFY_PASS); }
 
 extern "C" int ddtree_kv_compact(const void* kv_src, void* kv_dst, const int32_t* slot_idx,

@@ -26,9 +26,10 @@ struct PrefixParams {
   const uint16_t* q;         // bf16 [B, T, H, 576]
   const uint16_t* kv;        // bf16 [N, 576]
   const int32_t* slot_idx;   // [B, slot_stride]
-  const int32_t* prefix_len; // [B]
+  const int32_t* prefix_len; // [B], or null: every request has max_prefix_len keys
   int64_t pool_slots;
   int32_t slot_stride;
+  int32_t sparse;            // slot tables are index lists: -1 entries are "no key" (no status bit)
   int32_t rows;              // T * H rows per request (the row stride of q)
   int32_t heads;             // H
   int32_t nodes;             // T
@@ -51,7 +52,8 @@ struct PrefixParams {
 struct TailParams {
   const uint16_t* q;
   const uint16_t* kv;
-  const int32_t* prefix_len;
+  const int32_t* prefix_len;    // [B], or null: every request has max_prefix_len keys
+  int32_t no_tail;              // no tree part: the rows are merged from the prefix partials alone
   const int32_t* tree_parent;   // [B, T]
   const int32_t* tree_slot_idx; // [B, T]
   int64_t pool_slots;

@@ -344,7 +344,9 @@ __device__ __forceinline__ int run_unit(const PrefixParams& p, Shared& sh, uint8
       const int kbase = kbegin + j * kNk;
       const bool v0 = kbase + lane < kend && in_pool(cur0), v1 = kbase + lane + 32 < kend && in_pool(cur1);
       if (warp == 1 && rank == 0) {
-        const bool bad0 = kbase + lane < kend && !in_pool(cur0), bad1 = kbase + lane + 32 < kend && !in_pool(cur1);
+        // (index lists: a -1 entry is no key, not a bad slot)
+        const bool bad0 = kbase + lane < kend && !in_pool(cur0) && !(p.sparse && cur0 == -1);
+        const bool bad1 = kbase + lane + 32 < kend && !in_pool(cur1) && !(p.sparse && cur1 == -1);
         if (__any_sync(0xffffffffu, bad0 || bad1) && lane == 0) atomicOr(p.status, kStatusBadSlot);
       }
       const bool all_valid = __all_sync(0xffffffffu, v0 && v1);
@@ -795,7 +797,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
   const int split = blockIdx.y;
   const int b = blockIdx.z;
 
-  int L = __ldg(p.prefix_len + b);
+  int L = p.prefix_len != nullptr ? __ldg(p.prefix_len + b) : p.max_prefix_len;
   if (L < 0 || L > p.max_prefix_len) {
     if (tid == 0 && rank == 0 && split == 0 && row_tile == 0) atomicOr(p.status, kStatusBadPrefix);
     L = L < 0 ? 0 : p.max_prefix_len;
@@ -957,7 +959,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) verify_
     const int split = (u / p.row_tiles) % f.splits;
     const int b = u / (p.row_tiles * f.splits);
     const bool first = split == 0 && tile == 0 && rank == 0 && tid == 0;  // reports the request's status bits
-    int L = __ldg(p.prefix_len + b);
+    int L = p.prefix_len != nullptr ? __ldg(p.prefix_len + b) : p.max_prefix_len;
     if (L < 0 || L > p.max_prefix_len) {
       if (first) atomicOr(p.status, kStatusBadPrefix);
       L = L < 0 ? 0 : p.max_prefix_len;

@@ -60,12 +60,13 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
   }
 
   // the request's parent and slot arrays, loaded in parallel, then one walk in smem
-  for (int i = tid; i < T; i += kTailThreads) {
+  for (int i = tid; i < T && !p.no_tail; i += kTailThreads) {
     par_sh[i] = __ldg(p.tree_parent + static_cast<int64_t>(b) * T + i);
     tslot_sh[i] = __ldg(p.tree_slot_idx + static_cast<int64_t>(b) * T + i);
   }
   __syncthreads();
-  if (tid == 0) {
+  if (tid == 0 && p.no_tail) n_vis_sh = 0;
+  if (tid == 0 && !p.no_tail) {
     int32_t st = 0;
     n_vis_sh = ancestor_slots(t, T, p.pool_slots, [&](int u) { return par_sh[u]; }, [&](int u) { return tslot_sh[u]; },
                               vis_slot_sh, &st);
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
   }
   __syncthreads();
 
-  int L = __ldg(p.prefix_len + b);
+  int L = p.prefix_len != nullptr ? __ldg(p.prefix_len + b) : p.max_prefix_len;
   L = L < 0 ? 0 : (L > p.max_prefix_len ? p.max_prefix_len : L);
   const int splits = (L + p.chunk - 1) / p.chunk;
   const int h = blockIdx.y * p.heads_per_cta + warp;

@@ -28,7 +28,7 @@ EXPORTS = ("ddtree_verify_workspace_bytes", "ddtree_verify_attn", "ddtree_verify
            "ddtree_verify_attn_ragged",
            "ddtree_verify_prefix_phase",
            "ddtree_verify_merge_phase", "ddtree_verify_attn_static_scratch", "ddtree_kv_compact",
-           "ddtree_kv_compact_check",
+           "ddtree_kv_compact_check", "ddtree_verify_sparse_workspace_bytes", "ddtree_verify_attn_sparse",
            "ddtree_read_device_status", "ddtree_status_string")
 
 
@@ -78,6 +78,12 @@ def load(path: str):
         L.ddtree_kv_compact_check.restype = ctypes.c_int
         L.ddtree_kv_compact_check.argtypes = [vp, vp, vp, vp, ctypes.POINTER(Dims), ctypes.c_int32,
                                               ctypes.POINTER(ctypes.c_int64)]
+    if hasattr(L, "ddtree_verify_attn_sparse"):
+        L.ddtree_verify_sparse_workspace_bytes.restype = ctypes.c_size_t
+        L.ddtree_verify_sparse_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+        L.ddtree_verify_attn_sparse.restype = ctypes.c_int
+        L.ddtree_verify_attn_sparse.argtypes = [vp, vp, i32p, ctypes.c_float, vp, vp, ctypes.POINTER(Dims), vp,
+                                                ctypes.c_size_t, vp]
     L.ddtree_read_device_status.restype = ctypes.c_int
     L.ddtree_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
     L.ddtree_status_string.restype = ctypes.c_char_p
@@ -184,6 +190,41 @@ def verify_attn(q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm
     B, T, H, _ = q.shape
     v = Verifier(B, T, H, kv_pool.shape[0], slot_idx.shape[1], max_prefix_len, device=q.device)
     return v(q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out, lse, stream)
+
+
+class SparseVerifier:
+    """Sparse-index verify attention: node (b, t) attends to the pool rows its index list names.
+
+    indices [B, T, topk] int32 CUDA tensor (-1 = no key); q [B, T, H, 576] bf16; a workspace is
+    held for one set of sizes.
+    """
+
+    def __init__(self, batch, nodes, heads, pool_slots, topk, device=None, library=None):
+        import torch
+        self.lib = lib() if library is None else library
+        self.dims = make_dims(batch, nodes, heads, pool_slots, topk, topk)
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        with torch.cuda.device(self.device):
+            n = int(self.lib.ddtree_verify_sparse_workspace_bytes(ctypes.byref(self.dims)))
+            if n == 0:
+                raise DDTError(-2, "ddtree_verify_sparse_workspace_bytes")
+            self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device)
+
+    def __call__(self, q, kv_pool, indices, sm_scale, out=None, lse=None, stream=None):
+        import torch
+        B, T, H, _ = q.shape
+        if out is None:
+            out = torch.empty((B, T, H, D_V), dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+        rc = self.lib.ddtree_verify_attn_sparse(_ptr(q), _ptr(kv_pool), _ptr(indices), float(sm_scale), _ptr(out),
+                                                _ptr(lse), ctypes.byref(self.dims), _ptr(self.workspace),
+                                                self.workspace.numel(), _stream(stream))
+        _check(rc, "ddtree_verify_attn_sparse")
+        return out, lse
+
+    def status(self, stream=None) -> int:
+        return read_device_status(self.workspace, stream, library=self.lib)
 
 
 def verify_attn_static_scratch(q, kv_pool, slot_idx, prefix_len, tree_parent, tree_slot_idx, sm_scale, out,

@@ -446,3 +446,40 @@ def closed_case(kind: str, seed: int = 0xDD7EC000) -> Workload:
         w.kv_prefix_bits = rows
     w.name = f"closed:{kind}"
     return w
+
+
+# ----------------------------------------------------------------------------- sparse-index lists
+
+def sparse_indices(w: Workload, topk: int, seed: int = 0xDD7E5000, none_frac: float = 0.1,
+                   dup_frac: float = 0.05) -> np.ndarray:
+    """Random index lists for the sparse-index variant: int32 [B, T, topk].
+
+    Node (b, t) gets topk entries drawn from its request's own rows (prefix and
+    tree slots): about none_frac of them -1 (no key) and dup_frac repeats of an
+    entry already in the list; the rest distinct rows.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = np.full((w.batch, w.nodes, topk), -1, dtype=np.int32)
+    for b in range(w.batch):
+        rows = np.concatenate([w.slot_idx[b, :w.prefix_len[b]], w.tree_slot_idx[b]]).astype(np.int32)
+        for t in range(w.nodes):
+            n_valid = min(len(rows), int(round(topk * (1.0 - none_frac))))
+            n_dup = min(n_valid, int(round(topk * dup_frac)))
+            pick = rng.choice(rows, size=n_valid - n_dup, replace=False)
+            dups = rng.choice(pick, size=n_dup, replace=True) if n_dup and len(pick) else np.zeros(0, np.int32)
+            lst = np.concatenate([pick, dups, np.full(topk - len(pick) - len(dups), -1, np.int32)])
+            out[b, t] = rng.permutation(lst)
+    return out
+
+
+def compact_indices(w: Workload, indices: np.ndarray) -> np.ndarray:
+    """The same lists as rows of w.compact_host_pool() (-1 stays -1)."""
+    _, si, ts = w.compact_host_pool()
+    remap = {}
+    for b in range(w.batch):
+        L = int(w.prefix_len[b])
+        remap.update(zip(w.slot_idx[b, :L].tolist(), si[b, :L].tolist()))
+        remap.update(zip(w.tree_slot_idx[b].tolist(), ts[b].tolist()))
+    remap[-1] = -1
+    flat = np.asarray([remap[int(x)] for x in indices.reshape(-1)], dtype=np.int32)
+    return flat.reshape(indices.shape)
