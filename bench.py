@@ -90,6 +90,8 @@ def job_throughput_gbs(kv_bytes_per_step, steps, world, max_ms):
 
 def workload_config(w, name, layout, ragged=0, warm_l2=False):
     desc = f"{name}: {wl.DESCRIPTIONS[name]}"
+    if w.pool_slots != wl.CONFIGS[name].pool_slots:
+        desc += f"; pool resized to {w.pool_slots} slots"
     if ragged:
         desc += f"; ragged trees, tree_len per request seeded U[{min(ragged, w.nodes)}, {w.nodes}]"
     return {"workload": desc, "batch": w.batch, "prefix_len_total": int(w.prefix_len.sum()),
@@ -217,7 +219,7 @@ def roofline_of(w, kernel_s, peaks):
     return bound, w.algorithmic_bytes() / kernel_s / 1e9, peaks["hbm_gbs"], "GB/s"
 
 
-def time_config(name, args, dev, world, layout=None, ragged=0, flush=None):
+def time_config(name, args, dev, world, layout=None, ragged=0, flush=None, pool_slots=None):
     """Device time of verify steps on one configuration (inputs resident in HBM).
 
     Returns a dict with the workload, its tensors and the measured times; the
@@ -227,7 +229,7 @@ def time_config(name, args, dev, world, layout=None, ragged=0, flush=None):
     from speculative_decoding_tree_05_gb300 import ddtree
 
     layout = layout or wl.CONFIGS[name].slots
-    w = wl.make_workload(name, slots=layout)
+    w = wl.make_workload(name, slots=layout, **({"pool_slots": pool_slots} if pool_slots else {}))
     tl_dev = None
     if ragged:
         # ragged trees: request b keeps its first tree_len[b] nodes, tree_len seeded uniform in [MIN, T]
@@ -306,7 +308,8 @@ def run_ours(args, rank, world, local_rank):
     name = args.config
     peaks, peak_kind = load_peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    cfg = time_config(name, args, dev, world, layout=args.slots, ragged=args.ragged, flush=flush)
+    cfg = time_config(name, args, dev, world, layout=args.slots, ragged=args.ragged, flush=flush,
+                      pool_slots=args.pool_slots)
     w, d, v, out, lse, stream = cfg["w"], cfg["d"], cfg["v"], cfg["out"], cfg["lse"], cfg["stream"]
 
     clocks = ClockSampler(local_rank)
@@ -412,6 +415,8 @@ def main():
                     help="comma-separated configurations also timed in the same run (per_config); '' for none")
     ap.add_argument("--slots", choices=["perm", "churn", "contiguous"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-slots", type=int, default=None,
+                    help="override the measured workload's pool size (profiling on a small device footprint)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="--impl reference: seconds of timed oracle work after which no further step starts")
