@@ -58,10 +58,10 @@ def source_digest(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(workload):
-    """DRAM bytes per prefix-kernel launch from a committed ncu summary, if it was
+def recorded_traffic(workload, kernel="prefix_pair_kernel"):
+    """DRAM bytes per prefix-kernel launch from a committed ncu summary of that kernel, if it was
     taken on the current kernel source; else None."""
-    path = os.path.join(PROFILE_DIR, f"prefix_pair_{workload}.txt")
+    path = os.path.join(PROFILE_DIR, f"{kernel.replace('_kernel', '')}_{workload}.txt")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -258,7 +258,10 @@ def time_config(name, args, dev, world, layout=None, ragged=0, flush=None, pool_
         step([torch.cuda.Event(enable_timing=True) for _ in range(2)])
     torch.cuda.synchronize(dev)
     assert v.status() == 0
-    return dict(w=w, d=d, v=v, out=out, lse=lse, stream=stream, step=step, tl_dev=tl_dev, layout=layout)
+    # the prefix pass runs as key-range groups or as fixed-length splits (two kernels)
+    kernel = "prefix_group_kernel" if ddtree.plan(v.dims)["groups"] > 0 else "prefix_pair_kernel"
+    return dict(w=w, d=d, v=v, out=out, lse=lse, stream=stream, step=step, tl_dev=tl_dev, layout=layout,
+                kernel=kernel)
 
 
 def timed_steps(cfg, n):
@@ -293,9 +296,9 @@ def summary_of(cfg, step_ms, prefix_ms, peaks, peak_kind, ragged=0):
         "kv_gbs": w.kv_bytes() / (ms * 1e-3) / 1e9,
         "roofline_step": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (ms * 1e-3), "bound": bound,
                           "peaks": peak_kind},
-        "roofline": {"kernel": "verify step (prefix + merge)" if ragged else "prefix_pair_kernel",
+        "roofline": {"kernel": "verify step (prefix + merge)" if ragged else cfg["kernel"],
                      "bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "traffic": None if ragged else recorded_traffic(w.name),
+                     "traffic": None if ragged else recorded_traffic(w.name, cfg["kernel"]),
                      "peak_kind": f"{peak_kind} (burst)", "kernel_us": statistics.mean(prefix_ms) * 1e3},
     }
 

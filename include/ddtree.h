@@ -124,9 +124,12 @@ DDT_API size_t ddtree_verify_workspace_bytes(const ddt_dims* dims);
  * ancestor rule; a log-sum-exp merge combines them.  The call enqueues a
  * workspace clear, the prefix pass and the tail/merge kernel (exactly
  * ddtree_verify_prefix_phase then ddtree_verify_merge_phase; the second kernel
- * starts as a programmatic dependent of the first).  ddtree_verify_attn_fused
- * computes the same bits in one launch.  Capturable in a CUDA graph.  B = 0
- * enqueues nothing and returns DDT_OK.
+ * starts as a programmatic dependent of the first).  The key ranges come from
+ * the sizes and the SM count: fixed-length splits of every request, or, for a
+ * batch of 2 to 64 requests whose row tiles fit at least twice on the GPU's
+ * CTA pairs, key-range groups (the requests' keys laid end to end and cut into
+ * equal shares, each computed by one group of pairs).  Capturable in a CUDA
+ * graph.  B = 0 enqueues nothing and returns DDT_OK.
  */
 DDT_API int ddtree_verify_attn(const void* q, const void* kv_pool, const int32_t* slot_idx,
                        const int32_t* prefix_len, const int32_t* tree_parent,
@@ -143,8 +146,11 @@ DDT_API int ddtree_verify_attn(const void* q, const void* kv_pool, const int32_t
  * works through the (request, key split, 128-row tile) units; the pair that
  * finishes the last split of a (request, row tile) merges its rows (tree tail
  * and log-sum-exp merge), counted with an atomic in the workspace: nothing ever
- * waits on another pair.  Same arguments, checks and results (bit for bit) as
- * ddtree_verify_attn.  It is slower than ddtree_verify_attn's two launches (the
+ * waits on another pair.  Same arguments and checks as ddtree_verify_attn, and
+ * the same bits wherever ddtree_verify_attn uses fixed-length splits (this
+ * launch always does; with key-range groups the partial sums are cut at other
+ * keys and the results agree within rounding).  It is slower than
+ * ddtree_verify_attn's two launches (the
  * merges run on the pairs that finish row tiles, not on every SM), so it is for
  * callers that want the single launch.
  */

@@ -9,6 +9,7 @@
 #include <vector>
 #include "../../include/ddtree.h"
 #include "kernels.cuh"
+#include "schedule.cuh"
 
 namespace ddt {
 namespace {
@@ -47,6 +48,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Plan {
   int rows = 0, row_tiles = 0, chunk = kKeysPerTile, splits = 0;
+  int groups = 0;  // > 0: the two-launch path divides the batch into this many key-range groups
   size_t cnt_off = 0, cnt_bytes = 0, lse_off = 0, o_off = 0, bytes = 0;
 };
 
@@ -104,8 +106,23 @@ int make_plan(const ddt_dims* d, int sm_count, Plan* plan) {
     int64_t chunk = (tiles + best - 1) / best * kKeysPerTile;
     p.chunk = static_cast<int>(chunk);
     p.splits = static_cast<int>((L + chunk - 1) / chunk);
+    // Key-range groups (schedule.cuh) for a batch whose row tiles fit at least
+    // twice into the pairs: groups of row_tiles pairs share the steps of all
+    // requests evenly, whatever their lengths.  Modelled cost: the steps of one
+    // group plus a unit's fixed cost per request it touches (one, plus the
+    // request boundaries that fall into it).  Taken when it is below the
+    // splits' cost.
+    if (d->batch >= 2 && d->batch <= kMaxGroupBatch && 2 * int64_t(p.row_tiles) <= pairs) {
+      const int64_t steps_all = len_sum > 0 ? (len_sum + kKeysPerTile - 1) / kKeysPerTile + d->batch / 2
+                                            : int64_t(d->batch) * tiles;
+      int64_t g = pairs / p.row_tiles;
+      g = std::min(g, std::max<int64_t>(1, steps_all / (kMinChunk / kKeysPerTile)));
+      const int64_t cost = (steps_all + g - 1) / g + kUnitOverheadSteps * (1 + (d->batch - 1 + g - 1) / g);
+      if (cost < best_cost) p.groups = static_cast<int>(g);
+    }
   }
-  const size_t part_rows = size_t(d->batch) * p.splits * p.row_tiles * kTileRows;
+  // split slots per request: the splits, or the pieces of the groups (at most one per group)
+  const size_t part_rows = size_t(d->batch) * std::max(p.splits, p.groups) * p.row_tiles * kTileRows;
   // [status words | split arrivals per (request, row tile) | lse partials | o partials]
   p.cnt_off = kStatusBytes;
   p.cnt_bytes = size_t(d->batch) * p.row_tiles * sizeof(int32_t);
@@ -265,7 +282,9 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
       pp.tree_len = tree_len;
       pp.row_tiles = plan.row_tiles;
       pp.chunk = plan.chunk;
-      pp.max_splits = plan.splits;
+      pp.max_splits = std::max(plan.splits, plan.groups);
+      pp.batch = dims->batch;
+      pp.groups = (phases & kPhaseFused) || sparse ? 0 : plan.groups;
       pp.max_prefix_len = dims->max_prefix_len;
       pp.scale_log2 = scale_log2;
       pp.o_part = o_part;
@@ -306,7 +325,9 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
     tp.heads_per_cta = dims->num_heads < 8 ? dims->num_heads : 8;
     tp.row_tiles = plan.row_tiles;
     tp.chunk = plan.chunk;
-    tp.max_splits = plan.splits;
+    tp.max_splits = std::max(plan.splits, plan.groups);
+    tp.batch = dims->batch;
+    tp.groups = sparse ? 0 : plan.groups;
     tp.max_prefix_len = dims->max_prefix_len;
     tp.scale_log2 = scale_log2;
     tp.o_part = o_part;
@@ -456,6 +477,47 @@ extern "C" int ddtree_read_device_status(const void* workspace, int32_t* host_st
   if (cudaMemcpy(host_status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
     return DDT_ERR_LAUNCH;
   return DDT_OK;
+}
+
+// Host-side introspection of the schedule (not part of the public header; the
+// CPU tests use it, no device is needed).
+// The plan for these sizes on a device with sm_count SMs: out = {row tiles,
+// key splits, keys per split, key-range groups (0: splits)}.
+extern "C" __attribute__((visibility("default"))) int ddtree_internal_plan(const ddt_dims* dims, int sm_count,
+                                                                           int32_t* out) {
+  Plan plan;
+  const int rc = make_plan(dims, sm_count, &plan);
+  if (rc != DDT_OK) return rc;
+  out[0] = plan.row_tiles;
+  out[1] = plan.splits;
+  out[2] = plan.chunk;
+  out[3] = plan.groups;
+  return DDT_OK;
+}
+
+// Unit idx of key-range group g for host-side prefix lengths (clamped to
+// [0, max_len] like the kernels do): out = {request, kbegin, kend, piece};
+// returns 1, or 0 once the group has no more units.  With g < 0 it returns
+// instead, in out[0], the number of pieces (split slots) of request idx.
+extern "C" __attribute__((visibility("default"))) int ddtree_internal_group_unit(const int32_t* prefix_len, int batch,
+                                                                                 int max_len, int groups, int g,
+                                                                                 int idx, int32_t* out) {
+  std::vector<int64_t> first(batch + 1, 0);
+  std::vector<int> len(batch);
+  for (int b = 0; b < batch; ++b) {
+    const int L = prefix_len[b];
+    len[b] = L < 0 ? 0 : (L > max_len ? max_len : L);
+    first[b + 1] = first[b] + (len[b] + kKeysPerTile - 1) / kKeysPerTile;
+  }
+  const int64_t K = first[batch];
+  auto off = [&](int r) { return first[r]; };
+  auto steps = [&](int r) { return first[r + 1] - first[r]; };
+  auto keys = [&](int r) { return len[r]; };
+  if (g < 0) {
+    out[0] = group_pieces(off(idx), steps(idx), K, groups);
+    return 1;
+  }
+  return nth_group_unit(g, groups, K, batch, idx, off, steps, keys, &out[0], &out[1], &out[2], &out[3]) ? 1 : 0;
 }
 
 #ifdef DDT_TEST_HOOKS

@@ -35,8 +35,10 @@ struct PrefixParams {
   int32_t nodes;             // T
   const int32_t* tree_len;   // [B] active nodes per request, or null: all T active
   int32_t row_tiles;         // ceil(rows / 128)
-  int32_t chunk;             // keys per split
+  int32_t chunk;             // keys per split (groups == 0)
   int32_t max_splits;        // split slots per request in the workspace
+  int32_t batch;             // B
+  int32_t groups;            // > 0: key-range groups (schedule.cuh; batch <= 64), grid (2 row_tiles, groups)
   int32_t max_prefix_len;
   float scale_log2;          // sm_scale * log2(e)
   int32_t block_loads;       // tmap_block and tmap_rope are valid (pool has >= 64 rows)
@@ -62,8 +64,10 @@ struct TailParams {
   const int32_t* tree_len;      // [B] active nodes per request, or null: all T active
   int32_t heads_per_cta;
   int32_t row_tiles;
-  int32_t chunk;
+  int32_t chunk;                // keys per split (groups == 0)
   int32_t max_splits;
+  int32_t batch;                // B
+  int32_t groups;               // > 0: the prefix pass ran key-range groups: request b has its pieces' partials
   int32_t max_prefix_len;
   float scale_log2;
   const float* o_part;
@@ -100,16 +104,18 @@ struct CompactParams {
   int32_t* status;
 };
 
-// Prefix kernel geometry: a pair of CTAs per 128-row tile, 32 keys per step.
+// Prefix kernel geometry: a pair of CTAs per 128-row tile, 64 keys per step.
 constexpr int kTileRows = 128;            // query rows per CTA pair (tcgen05 M)
 constexpr int kKeysPerTile = 64;          // keys per pipeline step
 constexpr int kMinChunk = 256;            // shortest key split the planner makes
 constexpr int kUnitOverheadSteps = 6;     // fixed cost of one prefix unit, in 64-key steps (measured)
+constexpr int kMaxGroupBatch = 64;        // key-range groups take batches up to this size (one warp's table)
 
 // Per-device set-up (shared-memory opt-in), called once per device before launches.
 cudaError_t configure_prefix();
 cudaError_t configure_tail_merge();
 
+// grid (2 row_tiles, splits, batch), or (2 row_tiles, groups) when p.groups > 0
 cudaError_t launch_prefix(const PrefixParams& p, int batch, int splits, cudaStream_t stream);
 // pairs: CTA pairs of the persistent grid (at most the clusters that fit at once)
 cudaError_t launch_fused(const FusedParams& p, int pairs, cudaStream_t stream);

@@ -92,6 +92,7 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include "kernels.cuh"
+#include "schedule.cuh"
 #include "merge_row.cuh"
 #include "ptx.cuh"
 
@@ -135,7 +136,6 @@ constexpr float kRescaleThreshold = 8.f;                 // log2 units
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr int kXFracBits = 18;                           // 20-bit mantissa = round(x * 2^(18-e)) + 2^19
 constexpr float kMagic = 13107200.0f;                    // 1.5 * 2^23 + 2^19
-constexpr uint32_t kMagicHi = 0x4B4B4B4Bu;               // top byte of every encoded float, repeated
 constexpr int kXFracBits16 = 14;                         // 16-bit mantissa = round(x * 2^(14-e)) + 2^15
 constexpr float kMagic16 = 12615680.0f;                  // 1.5 * 2^23 + 2^15
 constexpr uint32_t kMagicHi16 = 0x4B400000u;             // top half of every 16-bit-encoded float
@@ -836,6 +836,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
   }
 }
 
+// The prefix pass by key-range groups (schedule.cuh): the pair (row tile
+// blockIdx.x / 2, group blockIdx.y) computes its row tile over the group's
+// steps, one unit per request that they touch, back to back on the same
+// barriers (their phases run on: the CTA's steps G and passes count across
+// units).  A unit's partial goes to its piece's split slot of the request.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_group_kernel(const __grid_constant__ PrefixParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Shared sh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  grid_dep_launch();  // as in prefix_pair_kernel
+  const int row_tile = blockIdx.x >> 1;
+  if (warp == 0) {
+    tmem_alloc(&sh.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) init_barriers(sh);
+  int G = 0, pass = 0;
+  for (int idx = 0;; ++idx) {
+    // the step table is rebuilt for each unit (two loads and a few shuffles per
+    // warp) instead of being held in registers across the unit
+    int b, kbegin, kend, piece;
+    {
+      const StepTable st = step_table(p.prefix_len, p.max_prefix_len, p.batch, lane);
+      if (idx == 0 && st.bad && blockIdx.y == 0 && row_tile == 0 && rank == 0 && tid == 0)
+        atomicOr(p.status, kStatusBadPrefix);
+      if (!nth_group_unit(
+              blockIdx.y, p.groups, st.total, p.batch, idx, [&](int r) { return st.off(r); },
+              [&](int r) { return st.steps(r); }, [&](int r) { return st.keys(r); }, &b, &kbegin, &kend, &piece))
+        break;
+    }
+    int rows_b = p.rows;
+    if (p.tree_len != nullptr) {
+      const int tl = __ldg(p.tree_len + b);
+      rows_b = (tl < 0 ? 0 : (tl > p.nodes ? p.nodes : tl)) * p.heads;  // out-of-range values: the merge reports them
+    }
+    if (row_tile * kTileRows >= rows_b) continue;  // inactive rows: both CTAs skip the unit
+    const int ntiles = (kend - kbegin + kNk - 1) / kNk;
+    int flags = run_unit<false>(p, sh, smem_raw, row_tile, piece, b, kbegin, kend, rows_b, G, pass);
+    G += ntiles;
+    ++pass;
+    if (flags == kUnitWide) {
+#ifdef DDT_TEST_HOOKS
+      if (tid == 0 && rank == 0) atomicAdd(p.status + 2, 1);  // test builds count the 20-bit reruns
+#endif
+      flags = run_unit<true>(p, sh, smem_raw, row_tile, piece, b, kbegin, kend, rows_b, G, pass);
+      G += ntiles;
+      ++pass;
+    }
+    if (flags & kUnitAborted) break;  // both CTAs of the pair stop (the status word says TIMEOUT)
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(sh.tmem_base, kTmemCols);
+  }
+}
+
 // Fused kernel: merge the rows of one (request, row tile): the tree tail of
 // each row and the log-sum-exp merge with the request's nsplit prefix partials.
 // Rank r of the pair takes rows [64 r, 64 r + 64) of the tile, a warp every
@@ -1023,6 +1080,8 @@ int g_fused_pairs[64];  // co-resident pairs per device, found once by configure
 cudaError_t configure_prefix() {
   cudaError_t e = cudaFuncSetAttribute(prefix_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(prefix_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess)
+    return e;
   if ((e = cudaFuncSetAttribute(verify_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess)
     return e;
   int dev = 0;
@@ -1052,8 +1111,11 @@ cudaError_t launch_fused(const FusedParams& p, int pairs, cudaStream_t stream) {
 }
 
 cudaError_t launch_prefix(const PrefixParams& p, int batch, int splits, cudaStream_t stream) {
-  dim3 grid(2 * p.row_tiles, splits, batch);
-  prefix_pair_kernel<<<grid, kThreads, kSmem, stream>>>(p);
+  if (p.groups > 0) {
+    prefix_group_kernel<<<dim3(2 * p.row_tiles, p.groups, 1), kThreads, kSmem, stream>>>(p);
+  } else {
+    prefix_pair_kernel<<<dim3(2 * p.row_tiles, splits, batch), kThreads, kSmem, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

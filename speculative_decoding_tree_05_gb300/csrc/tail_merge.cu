@@ -25,6 +25,7 @@
 #include "kernels.cuh"
 #include "merge_row.cuh"
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 namespace ddt {
 namespace {
@@ -81,9 +82,17 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
   }
   __syncthreads();
 
-  int L = p.prefix_len != nullptr ? __ldg(p.prefix_len + b) : p.max_prefix_len;
-  L = L < 0 ? 0 : (L > p.max_prefix_len ? p.max_prefix_len : L);
-  const int splits = (L + p.chunk - 1) / p.chunk;
+  // the prefix partials of request b: its key splits, or with key-range groups
+  // the groups its steps span (pieces 0.. in the request's split slots)
+  int splits;
+  if (p.groups > 0) {
+    const StepTable st = step_table(p.prefix_len, p.max_prefix_len, p.batch, lane);
+    splits = group_pieces(st.off(b), st.steps(b), st.total, p.groups);
+  } else {
+    int L = p.prefix_len != nullptr ? __ldg(p.prefix_len + b) : p.max_prefix_len;
+    L = L < 0 ? 0 : (L > p.max_prefix_len ? p.max_prefix_len : L);
+    splits = (L + p.chunk - 1) / p.chunk;
+  }
   const int h = blockIdx.y * p.heads_per_cta + warp;
   if (warp >= p.heads_per_cta || h >= p.heads) return;
 

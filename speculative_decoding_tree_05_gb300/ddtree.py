@@ -84,6 +84,9 @@ def load(path: str):
         L.ddtree_verify_attn_sparse.restype = ctypes.c_int
         L.ddtree_verify_attn_sparse.argtypes = [vp, vp, i32p, ctypes.c_float, vp, vp, ctypes.POINTER(Dims), vp,
                                                 ctypes.c_size_t, vp]
+    if hasattr(L, "ddtree_internal_plan"):
+        L.ddtree_internal_plan.restype = ctypes.c_int
+        L.ddtree_internal_plan.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.POINTER(ctypes.c_int32)]
     L.ddtree_read_device_status.restype = ctypes.c_int
     L.ddtree_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
     L.ddtree_status_string.restype = ctypes.c_char_p
@@ -121,6 +124,17 @@ def make_dims(batch, nodes, heads, pool_slots, slot_stride, max_prefix_len, pref
 
 def workspace_bytes(dims: Dims) -> int:
     return int(lib().ddtree_verify_workspace_bytes(ctypes.byref(dims)))
+
+
+def plan(dims: Dims, sm_count: int | None = None, library=None) -> dict:
+    """The schedule the library picks for these sizes: row tiles, key splits and keys per split, or
+    key-range groups (groups > 0).  sm_count: the device's SM count (default: the current device's)."""
+    if sm_count is None:
+        import torch
+        sm_count = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    out = (ctypes.c_int32 * 4)()
+    _check((library or lib()).ddtree_internal_plan(ctypes.byref(dims), int(sm_count), out), "ddtree_internal_plan")
+    return dict(row_tiles=out[0], splits=out[1], chunk=out[2], groups=out[3])
 
 
 def _check(rc, what):

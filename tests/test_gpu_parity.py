@@ -238,7 +238,8 @@ def test_fused_launch_equals_the_two_phases(kw):
 @pytest.mark.parametrize("name", ["c3", "c5"])
 def test_fused_launch_full_size(name):
     # multi-wave configurations of the single fused launch: every element against the oracle, and the
-    # same bits as the two-launch path
+    # same bits as the two-launch path where that path uses the same fixed-length key splits (c3; the
+    # batch of c5 is divided by key-range groups there, which cut the keys elsewhere)
     w = wl.make_workload(name)
     d = wl.to_device(w, "cuda", poison=True)
     v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len)
@@ -247,6 +248,10 @@ def test_fused_launch_full_size(name):
     assert v.status() == 0
     o2, l2 = v(*args, phase="prefix")
     o2, l2 = v(*args, out=o2, lse=l2, phase="merge")
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert v.status() == 0
     ref_o, ref_l, _ = oracle_full(name)
     compare(o1, l1, ref_o, ref_l)
+    if ddtree.plan(v.dims)["groups"] == 0:
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    else:
+        compare(o2, l2, ref_o, ref_l)
