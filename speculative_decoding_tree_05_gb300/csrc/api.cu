@@ -47,7 +47,7 @@ int device_info(DeviceInfo* out) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Plan {
-  int rows = 0, row_tiles = 0, chunk = kKeysPerTile, splits = 0;
+  int rows = 0, row_tiles = 0, chunk0 = kKeysPerTile, chunk = kKeysPerTile, splits = 0;
   int groups = 0;  // > 0: the two-launch path divides the batch into this many key-range groups
   size_t cnt_off = 0, cnt_bytes = 0, lse_off = 0, o_off = 0, bytes = 0;
 };
@@ -104,8 +104,24 @@ int make_plan(const ddt_dims* d, int sm_count, Plan* plan) {
       }
     }
     int64_t chunk = (tiles + best - 1) / best * kKeysPerTile;
-    p.chunk = static_cast<int>(chunk);
-    p.splits = static_cast<int>((L + chunk - 1) / chunk);
+    p.chunk0 = p.chunk = static_cast<int>(chunk);
+    // One request whose row tiles leave R pairs free (T < pairs): a long first
+    // split A on T pairs while the R others take the T short second splits,
+    // k = ceil(T / R) each.  Balanced when A + o = k (S - A + o) (S steps, o a
+    // unit's fixed cost); taken when its modelled time is below the equal
+    // splits'.  c3: 65 tiles on 76 pairs, 882 + 142 steps in 888 step times
+    // against 6 waves of 147 (918).
+    const int64_t T = p.row_tiles, R = pairs - T, o = kUnitOverheadSteps;
+    if (d->batch == 1 && R > 0 && tiles > 1) {
+      const int64_t k = (T + R - 1) / R;
+      const int64_t A = std::min(tiles - 1, std::max<int64_t>(1, (k * (tiles + o) - o + k) / (k + 1)));
+      const int64_t cost = std::max(A + o, k * (tiles - A + o));
+      if (cost < best_cost) {
+        p.chunk0 = static_cast<int>(A * kKeysPerTile);
+        p.chunk = static_cast<int>((tiles - A) * kKeysPerTile);
+      }
+    }
+    p.splits = split_count(static_cast<int>(L), p.chunk0, p.chunk);
     // Key-range groups (schedule.cuh) for a batch whose row tiles fit at least
     // twice into the pairs: groups of row_tiles pairs share the steps of all
     // requests evenly, whatever their lengths.  Modelled cost: the steps of one
@@ -281,6 +297,7 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
       pp.nodes = dims->num_nodes;
       pp.tree_len = tree_len;
       pp.row_tiles = plan.row_tiles;
+      pp.chunk0 = plan.chunk0;
       pp.chunk = plan.chunk;
       pp.max_splits = std::max(plan.splits, plan.groups);
       pp.batch = dims->batch;
@@ -324,6 +341,7 @@ int verify_phases(int phases, const void* q, const void* kv_pool, const int32_t*
     tp.tree_len = tree_len;
     tp.heads_per_cta = dims->num_heads < 8 ? dims->num_heads : 8;
     tp.row_tiles = plan.row_tiles;
+    tp.chunk0 = plan.chunk0;
     tp.chunk = plan.chunk;
     tp.max_splits = std::max(plan.splits, plan.groups);
     tp.batch = dims->batch;
@@ -482,7 +500,8 @@ extern "C" int ddtree_read_device_status(const void* workspace, int32_t* host_st
 // Host-side introspection of the schedule (not part of the public header; the
 // CPU tests use it, no device is needed).
 // The plan for these sizes on a device with sm_count SMs: out = {row tiles,
-// key splits, keys per split, key-range groups (0: splits)}.
+// key splits, keys of each later split, key-range groups (0: splits), keys of
+// split 0}.
 extern "C" __attribute__((visibility("default"))) int ddtree_internal_plan(const ddt_dims* dims, int sm_count,
                                                                            int32_t* out) {
   Plan plan;
@@ -492,6 +511,7 @@ extern "C" __attribute__((visibility("default"))) int ddtree_internal_plan(const
   out[1] = plan.splits;
   out[2] = plan.chunk;
   out[3] = plan.groups;
+  out[4] = plan.chunk0;
   return DDT_OK;
 }
 

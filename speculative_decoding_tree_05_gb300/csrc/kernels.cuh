@@ -35,7 +35,8 @@ struct PrefixParams {
   int32_t nodes;             // T
   const int32_t* tree_len;   // [B] active nodes per request, or null: all T active
   int32_t row_tiles;         // ceil(rows / 128)
-  int32_t chunk;             // keys per split (groups == 0)
+  int32_t chunk0;            // keys of split 0 (groups == 0; see split_begin)
+  int32_t chunk;             // keys of every later split
   int32_t max_splits;        // split slots per request in the workspace
   int32_t batch;             // B
   int32_t groups;            // > 0: key-range groups (schedule.cuh; batch <= 64), grid (2 row_tiles, groups)
@@ -64,7 +65,8 @@ struct TailParams {
   const int32_t* tree_len;      // [B] active nodes per request, or null: all T active
   int32_t heads_per_cta;
   int32_t row_tiles;
-  int32_t chunk;                // keys per split (groups == 0)
+  int32_t chunk0;               // keys of split 0 (groups == 0)
+  int32_t chunk;                // keys of every later split
   int32_t max_splits;
   int32_t batch;                // B
   int32_t groups;               // > 0: the prefix pass ran key-range groups: request b has its pieces' partials
@@ -110,6 +112,23 @@ constexpr int kKeysPerTile = 64;          // keys per pipeline step
 constexpr int kMinChunk = 256;            // shortest key split the planner makes
 constexpr int kUnitOverheadSteps = 6;     // fixed cost of one prefix unit, in 64-key steps (measured)
 constexpr int kMaxGroupBatch = 64;        // key-range groups take batches up to this size (one warp's table)
+
+// Fixed-length key splits of a request's prefix: split 0 holds keys
+// [0, chunk0), split s >= 1 keys [chunk0 + (s-1) chunk, +chunk), the last one
+// cut at the request's length L.  (chunk0 == chunk: equal splits; a longer
+// first split lets the row tiles' first units run on most pairs while the
+// remaining pairs work through the short splits.)
+__host__ __device__ inline int split_begin(int s, int chunk0, int chunk) {
+  return s == 0 ? 0 : chunk0 + (s - 1) * chunk;
+}
+__host__ __device__ inline int split_end(int s, int chunk0, int chunk, int L) {
+  const int64_t e = s == 0 ? chunk0 : chunk0 + int64_t(s) * chunk;
+  return e < L ? static_cast<int>(e) : L;
+}
+// number of splits that hold keys of a request with L keys
+__host__ __device__ inline int split_count(int L, int chunk0, int chunk) {
+  return L <= 0 ? 0 : (L <= chunk0 ? 1 : 1 + (L - chunk0 + chunk - 1) / chunk);
+}
 
 // Per-device set-up (shared-memory opt-in), called once per device before launches.
 cudaError_t configure_prefix();

@@ -802,7 +802,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     if (tid == 0 && rank == 0 && split == 0 && row_tile == 0) atomicOr(p.status, kStatusBadPrefix);
     L = L < 0 ? 0 : p.max_prefix_len;
   }
-  const int kbegin = split * p.chunk;
+  const int kbegin = split_begin(split, p.chunk0, p.chunk);
   if (kbegin >= L) return;  // both CTAs of the pair leave together
   // ragged trees: only the rows of the request's first tree_len[b] nodes are computed
   int rows_b = p.rows;
@@ -811,7 +811,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefix_
     rows_b = (tl < 0 ? 0 : (tl > p.nodes ? p.nodes : tl)) * p.heads;  // out-of-range values: the merge reports them
   }
   if (row_tile * kTileRows >= rows_b) return;  // a tile of inactive rows: both CTAs leave together
-  const int kend = min(L, kbegin + p.chunk);
+  const int kend = split_end(split, p.chunk0, p.chunk, L);
   // 16-bit exchange first; the rare unit whose partial scores are too large for
   // it (both CTAs get the same answer) is computed again with 20-bit mantissas
   // and its partial result overwritten
@@ -1030,14 +1030,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) verify_
       }
       rows_b = tl * p.heads;
     }
-    const int nsplit = (L + p.chunk - 1) / p.chunk;
+    const int nsplit = split_count(L, p.chunk0, p.chunk);
     if (tile * kTileRows >= rows_b || nsplit == 0) {
       if (split == 0) merge_tile(f, smem, b, tile, 0, rows_b);  // tree tail only, or inactive rows
       __syncthreads();
       continue;
     }
     if (split >= nsplit) continue;
-    const int kbegin = split * p.chunk, kend = min(L, kbegin + p.chunk);
+    const int kbegin = split_begin(split, p.chunk0, p.chunk), kend = split_end(split, p.chunk0, p.chunk, L);
     const int ntiles = (kend - kbegin + kNk - 1) / kNk;
     int flags = run_unit<false>(p, sh, smem_raw, tile, split, b, kbegin, kend, rows_b, G, pass);
     G += ntiles;

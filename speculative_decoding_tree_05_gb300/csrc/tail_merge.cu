@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_merge_kernel(TailParams p) 
   } else {
     int L = p.prefix_len != nullptr ? __ldg(p.prefix_len + b) : p.max_prefix_len;
     L = L < 0 ? 0 : (L > p.max_prefix_len ? p.max_prefix_len : L);
-    splits = (L + p.chunk - 1) / p.chunk;
+    splits = split_count(L, p.chunk0, p.chunk);
   }
   const int h = blockIdx.y * p.heads_per_cta + warp;
   if (warp >= p.heads_per_cta || h >= p.heads) return;

@@ -127,14 +127,14 @@ def workspace_bytes(dims: Dims) -> int:
 
 
 def plan(dims: Dims, sm_count: int | None = None, library=None) -> dict:
-    """The schedule the library picks for these sizes: row tiles, key splits and keys per split, or
-    key-range groups (groups > 0).  sm_count: the device's SM count (default: the current device's)."""
+    """The schedule the library picks for these sizes: row tiles, key splits (keys of split 0 and of
+    each later split), or key-range groups (groups > 0).  sm_count: the device's SM count (default: the current device's)."""
     if sm_count is None:
         import torch
         sm_count = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    out = (ctypes.c_int32 * 4)()
+    out = (ctypes.c_int32 * 5)()
     _check((library or lib()).ddtree_internal_plan(ctypes.byref(dims), int(sm_count), out), "ddtree_internal_plan")
-    return dict(row_tiles=out[0], splits=out[1], chunk=out[2], groups=out[3])
+    return dict(row_tiles=out[0], splits=out[1], chunk0=out[4], chunk=out[2], groups=out[3])
 
 
 def _check(rc, what):

@@ -136,3 +136,21 @@ def test_planner_takes_groups_for_a_mixed_batch(lib):
 ])
 def test_planner_keeps_splits(lib, kw):
     assert plan(lib, **kw)["groups"] == 0
+
+
+def test_planner_long_first_split_for_one_request_with_many_tiles(lib):
+    # 65 row tiles of one 65536-key request on 76 pairs: the 65 first units take 882 steps while the
+    # 11 free pairs run the 65 second units of 142 steps, six each (888 step times against 6 x 153)
+    p = plan(lib, batch=1, nodes=65, heads=128, pool_slots=2 << 20, slot_stride=65536, max_prefix_len=65536)
+    assert p["groups"] == 0 and p["splits"] == 2
+    assert (p["chunk0"], p["chunk"]) == (882 * STEP, 142 * STEP)
+    assert p["chunk0"] + p["chunk"] == 65536
+
+
+@pytest.mark.parametrize("kw,splits", [
+    (dict(batch=1, nodes=65, heads=16, pool_slots=1 << 20, slot_stride=8192, max_prefix_len=8192), 8),
+    (dict(batch=1, nodes=9, heads=16, pool_slots=4 << 20, slot_stride=185000, max_prefix_len=185000), 38),
+])
+def test_planner_equal_splits_when_tiles_are_few(lib, kw, splits):
+    p = plan(lib, **kw)
+    assert p["groups"] == 0 and p["splits"] == splits and p["chunk0"] == p["chunk"]
