@@ -105,3 +105,26 @@ def test_timeout_is_reported_and_the_next_call_is_correct(testhooks):
     assert st == 0
     ref_o, ref_l, _ = oracle.verify_workload(w)
     compare(out, lse, ref_o, ref_l)
+
+
+def test_timeout_in_a_key_range_group_plan(testhooks):
+    # the same under the key-range group schedule: a pair's units run back to back on one set of
+    # barriers, so after a wait runs out in one unit both CTAs of the pair must stop together
+    rng = np.random.default_rng(11)
+    lens = rng.integers(0, 3000, 64)
+    lens[:4] = (0, 1, 64, 2999)
+    w = wl.make_workload("tiny", batch=64, prefix=("list", *(int(x) for x in lens)), nodes=3, heads=16,
+                         max_depth=3, max_branch=0, pool_slots=1 << 18, slots="churn")
+    assert ddtree.plan(ddtree.make_dims(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride,
+                                        w.max_prefix_len))["groups"] > 0
+    d = wl.to_device(w, "cuda", poison=True)
+    testhooks.ddtree_test_set_drop_step(2)
+    try:
+        _, _, st, _, _ = run_gpu(w, dev=d, library=testhooks)
+    finally:
+        testhooks.ddtree_test_set_drop_step(-1)
+    assert st & ddtree.STATUS_TIMEOUT
+    out, lse, st, _, _ = run_gpu(w, dev=d, library=testhooks)
+    assert st == 0
+    ref_o, ref_l, _ = oracle.verify_workload(w)
+    compare(out, lse, ref_o, ref_l)
