@@ -255,3 +255,27 @@ def test_fused_launch_full_size(name):
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
     else:
         compare(o2, l2, ref_o, ref_l)
+
+
+# ----------------------------------------------------------------------------- long first split
+
+@pytest.mark.parametrize("length", [4096, 3900, 3840, 3841])
+def test_long_first_split_edges(length):
+    # 65 row tiles of one request under a bound of 4096 keys: the plan makes split 0 3840 keys long
+    # and split 1 256.  Prefixes that end inside split 0, at its end, and one key into split 1 (the
+    # merge must count 1, 1 and 2 splits) against the oracle, every element.
+    w = wl.make_workload("tiny", prefix=(length,), nodes=65, heads=128, max_depth=8, max_branch=4,
+                         pool_slots=1 << 14, slots="churn")
+    bound = 4096
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, bound, bound)
+    p = ddtree.plan(v.dims)
+    assert (p["groups"], p["splits"], p["chunk0"], p["chunk"]) == (0, 2, 3840, 256)
+    d = wl.to_device(w, "cuda", poison=True)
+    slots = torch.zeros((1, bound), dtype=torch.int32, device="cuda")  # the slot row padded to the bound
+    slots[:, :w.slot_stride] = d["slot_idx"]
+    d["slot_idx"] = slots
+    out, lse = v(d["q"], d["kv_pool"], d["slot_idx"], d["prefix_len"], d["tree_parent"], d["tree_slot_idx"],
+                 w.sm_scale)
+    assert v.status() == 0
+    ref_o, ref_l, _ = oracle.verify_workload(w)
+    compare(out, lse, ref_o, ref_l)
