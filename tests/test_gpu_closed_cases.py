@@ -128,3 +128,22 @@ def test_timeout_in_a_key_range_group_plan(testhooks):
     assert st == 0
     ref_o, ref_l, _ = oracle.verify_workload(w)
     compare(out, lse, ref_o, ref_l)
+
+
+def test_group_plan_reruns_with_wide_exchange(testhooks):
+    # queries scaled by 8 under the key-range group schedule: units rerun with 20-bit mantissas inside
+    # the persistent group kernel (the test build counts the reruns), and the product build agrees
+    rng = np.random.default_rng(12)
+    lens = rng.integers(500, 3000, 64)
+    w = wl.make_workload("tiny", batch=64, prefix=("list", *(int(x) for x in lens)), nodes=3, heads=16,
+                         max_depth=3, max_branch=0, pool_slots=1 << 18, slots="churn")
+    w.q_bits = wl.pow2_scaled_bits(w.q_bits, 3)
+    assert ddtree.plan(ddtree.make_dims(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride,
+                                        w.max_prefix_len))["groups"] > 0
+    d = wl.to_device(w, "cuda", poison=True)
+    out, lse, st, _, v = run_gpu(w, dev=d, library=testhooks)
+    assert st == 0 and _reruns(v) > 0
+    ref_o, ref_l, _ = oracle.verify_workload(w)
+    compare(out, lse, ref_o, ref_l)
+    out2, lse2, st2, _, _ = run_gpu(w, dev=d)
+    assert st2 == 0 and torch.equal(out, out2) and torch.equal(lse, lse2)
