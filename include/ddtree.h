@@ -125,7 +125,9 @@ DDT_API size_t ddtree_verify_workspace_bytes(const ddt_dims* dims);
  * workspace clear, the prefix pass and the tail/merge kernel (exactly
  * ddtree_verify_prefix_phase then ddtree_verify_merge_phase; the second kernel
  * starts as a programmatic dependent of the first).  The key ranges come from
- * the sizes and the SM count: fixed-length splits of every request, or, for a
+ * the sizes and the SM count: key splits of every request (all of one length,
+ * or, for one request whose row tiles leave CTA pairs free, a long first split
+ * with short ones behind it for the free pairs), or, for a
  * batch of 2 to 64 requests whose row tiles fit at least twice on the GPU's
  * CTA pairs, key-range groups (the requests' keys laid end to end and cut into
  * equal shares, each computed by one group of pairs).  Capturable in a CUDA
@@ -147,7 +149,7 @@ DDT_API int ddtree_verify_attn(const void* q, const void* kv_pool, const int32_t
  * finishes the last split of a (request, row tile) merges its rows (tree tail
  * and log-sum-exp merge), counted with an atomic in the workspace: nothing ever
  * waits on another pair.  Same arguments and checks as ddtree_verify_attn, and
- * the same bits wherever ddtree_verify_attn uses fixed-length splits (this
+ * the same bits wherever ddtree_verify_attn uses key splits (this
  * launch always does; with key-range groups the partial sums are cut at other
  * keys and the results agree within rounding).  It is slower than
  * ddtree_verify_attn's two launches (the
