@@ -421,13 +421,15 @@ def run_ours(args, rank, world, local_rank):
         if i >= args.warmup:
             serial_ms.append(s0.elapsed_time(s1))
     serial_s = statistics.mean(serial_ms) * 1e-3
-    e2e = {"value": kv_bytes * world / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-           "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
-           "loop": "copies in and back on two copy streams, double-buffered: a step's copies overlap its "
-                   "neighbours' kernels",
+    # the headline e2e is the serial loop (every step's copies and kernels in turn); the serving loop
+    # with the copies overlapped is reported beside it
+    e2e = {"value": kv_bytes * world / serial_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h), "ms_per_step": serial_s * 1e3, "steps": n_e2e,
+           "loop": "copy in, verify, read back, synchronise, one step at a time",
            "l2": "flushed before every step" if e2e_flush else "KV rows larger than twice the L2, not flushed",
-           "serial": {"value": kv_bytes * world / serial_s / 1e9, "ms_per_step": serial_s * 1e3,
-                      "loop": "copy in, verify, read back, synchronise, one step at a time"}}
+           "pipelined": {"value": kv_bytes * world / e2e_s / 1e9, "ms_per_step": e2e_s * 1e3,
+                         "loop": "copies in and back on two copy streams, double-buffered: a step's copies "
+                                 "overlap its neighbours' kernels"}}
     del cfg, d, v, dbuf, host
 
     # the other configurations, same protocol, reported under per_config
