@@ -142,3 +142,20 @@ def test_fused_launch_on_a_group_plan():
     assert v.status() == 0
     ref_o, ref_l, _ = oracle.verify_workload(w)
     compare(out, lse, ref_o, ref_l)
+
+
+def test_groups_clamp_and_report_prefix_lens_above_the_bound():
+    # a bound below some requests' lengths: the group kernel and the merge clamp those requests to the
+    # bound (the status word says so), and every row matches the oracle on the clamped lengths
+    w = _workload("many_small")
+    bound = 3000
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, bound)
+    assert ddtree.plan(v.dims)["groups"] > 0 and int(w.prefix_len.max()) > bound
+    d = wl.to_device(w, "cuda", poison=True)
+    out, lse = v(*_args(d, w))
+    assert v.status() == ddtree.STATUS_BAD_PREFIX
+    pool, si, ts = w.compact_host_pool()
+    clamped = np.minimum(w.prefix_len, bound).astype(w.prefix_len.dtype)
+    ref_o, ref_l, st = oracle.verify_attn(w.q_bits, pool, si, clamped, w.tree_parent, ts, w.sm_scale)
+    assert st == 0
+    compare(out, lse, ref_o, ref_l)
