@@ -147,3 +147,25 @@ def test_group_plan_reruns_with_wide_exchange(testhooks):
     compare(out, lse, ref_o, ref_l)
     out2, lse2, st2, _, _ = run_gpu(w, dev=d)
     assert st2 == 0 and torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_timeout_under_the_fused_launch(testhooks):
+    # the single fused launch: after a wait runs out, the pair stops claiming units (its barriers'
+    # phases are unknown), the status word says TIMEOUT, and the next call is correct
+    w = wl.make_workload("tiny", prefix=(3000,), nodes=33, heads=16, max_depth=6, max_branch=4,
+                         pool_slots=1 << 16, slots="churn")
+    d = wl.to_device(w, "cuda", poison=True)
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len,
+                        library=testhooks)
+    args = (d["q"], d["kv_pool"], d["slot_idx"], d["prefix_len"], d["tree_parent"], d["tree_slot_idx"], w.sm_scale)
+    testhooks.ddtree_test_set_drop_step(2)
+    try:
+        v(*args, phase="fused")
+        st = v.status()
+    finally:
+        testhooks.ddtree_test_set_drop_step(-1)
+    assert st & ddtree.STATUS_TIMEOUT
+    out, lse = v(*args, phase="fused")
+    assert v.status() == 0
+    ref_o, ref_l, _ = oracle.verify_workload(w)
+    compare(out, lse, ref_o, ref_l)

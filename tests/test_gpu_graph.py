@@ -70,3 +70,38 @@ def test_verify_call_replays_in_cuda_graph():
     assert torch.equal(out_g, out_d2) and torch.equal(lse_g, lse_d2)
     assert not torch.equal(out_d2, out_d)  # the new q really changed the result
     assert np.isfinite(out_g.cpu().numpy()).all()
+
+
+def test_group_plan_replays_in_cuda_graph():
+    # a batch whose prefix pass runs as key-range groups (the persistent group kernel) captured and
+    # replayed: the same bits as a direct call, also after new prefix lengths are written in place
+    # (the groups are recomputed on the device from prefix_len at every replay)
+    from speculative_decoding_tree_05_gb300 import ddtree
+
+    rng = np.random.default_rng(21)
+    lens = rng.integers(0, 3000, 64)
+    w = wl.make_workload("tiny", batch=64, prefix=("list", *(int(x) for x in lens)), nodes=3, heads=16,
+                         max_depth=3, max_branch=0, pool_slots=1 << 18, slots="churn")
+    d = wl.to_device(w, "cuda", poison=True)
+    v = ddtree.Verifier(w.batch, w.nodes, w.heads, w.pool_slots, w.slot_stride, w.max_prefix_len)
+    assert ddtree.plan(v.dims)["groups"] > 0
+    shape = (w.batch, w.nodes, w.heads, wl.D_V)
+    out_g = torch.empty(shape, dtype=torch.float32, device="cuda")
+    lse_g = torch.empty(shape[:3], dtype=torch.float32, device="cuda")
+    v(*_args(d, w), out=out_g, lse=lse_g)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        v(*_args(d, w), out=out_g, lse=lse_g)
+    for step in range(2):
+        if step == 1:
+            # shorter prefixes, written into the captured length array (the slot rows stay valid)
+            d["prefix_len"].copy_(torch.div(d["prefix_len"], 2, rounding_mode="floor"))
+        out_g.zero_()
+        lse_g.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert v.status() == 0
+        out_d, lse_d = v(*_args(d, w))
+        torch.cuda.synchronize()
+        assert torch.equal(out_g, out_d) and torch.equal(lse_g, lse_d)
